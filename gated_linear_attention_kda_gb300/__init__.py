@@ -1,0 +1,180 @@
+"""KDA (Kimi Delta Attention) chunked forward pass for GB300 -- Python binding.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``libkda.so`` (built from ``csrc/``) through its C ABI
+(``include/kda.h``). PyTorch supplies device memory and the current stream.
+There is no fallback: importing this package fails when the library is
+missing, and every call raises when the library reports an error.
+
+The call follows the tensor contract of "FlashKDA Input Tensor Shapes and
+DTypes: Complete Specification for the Forward Pass": bf16 q, k, v, g
+``[B, T, H, 128]``, bf16 beta logits ``[B, T, H]``, fp32 ``A_log [H]`` and
+``dt_bias [H, 128]``, ``lower_bound`` in [-5, 0], optional bf16/fp32 states
+``[B|N, H, 128, 128]``, optional int64 ``cu_seqlens [N+1]`` with B = 1, and
+contiguous CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libkda.so is not built; run `python -m gated_linear_attention_kda_gb300._build` "
+        "(or __graft_entry__.build()) first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE", 4: "KDA_ERR_RANGE",
+          5: "KDA_ERR_STATE_MISMATCH", 6: "KDA_ERR_ALIGN", 7: "KDA_ERR_LAUNCH", 8: "KDA_ERR_DEVICE"}
+DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
+_P, _F, _I64, _I = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int
+FWD_ARGTYPES = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]
+_lib.kda_fwd.argtypes = FWD_ARGTYPES
+_lib.kda_fwd.restype = _I
+_lib.kda_fwd_host.argtypes = FWD_ARGTYPES
+_lib.kda_fwd_host.restype = _I
+_lib.kda_last_error.restype = ctypes.c_char_p
+_lib.kda_check_device_status.argtypes = [_P]
+_lib.kda_check_device_status.restype = _I
+_lib.kda_gate_scale.argtypes = [_F]
+_lib.kda_gate_scale.restype = _F
+_lib.kda_plan.argtypes = [_I64, _I, ctypes.POINTER(_I), ctypes.POINTER(_I64)]
+_lib.kda_plan.restype = _I
+_lib.kda_version.restype = _I
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        msg = _lib.kda_last_error().decode(errors="replace")
+        super().__init__(f"{self.name}: {msg}")
+
+
+def _raise(status: int):
+    if status != 0:
+        if status in (1, 2, 3, 4, 5, 6):
+            raise ValueError(str(KDAError(status)))
+        raise KDAError(status)
+
+
+def _state_code(t):
+    if t is None:
+        return DTYPE_NONE
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise ValueError(f"state tensors must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(name, t, dtype, shape, cuda=True):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not cuda and t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state, cu_seqlens, cuda):
+    if not isinstance(q, torch.Tensor) or q.dim() != 4 or not isinstance(v, torch.Tensor) or v.dim() != 4:
+        raise ValueError("q, k, g must be [B, T, H, K] and v, out [B, T, H, V]")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    for name, t, shp in (("q", q, (B, T, H, K)), ("k", k, (B, T, H, K)), ("g", g, (B, T, H, K)),
+                         ("v", v, (B, T, H, V)), ("out", out, (B, T, H, V)), ("beta", beta, (B, T, H))):
+        if t is None:
+            raise ValueError(f"{name} is required")
+        _check(name, t, torch.bfloat16, shp, cuda)
+    _check("A_log", A_log, torch.float32, (H,), cuda)
+    _check("dt_bias", dt_bias, torch.float32, (H, K), cuda)
+    N = 0
+    if cu_seqlens is not None:
+        _check("cu_seqlens", cu_seqlens, torch.int64, None, cuda)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be [N+1] with N >= 1")
+        N = cu_seqlens.numel() - 1
+    S = N if cu_seqlens is not None else B
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        _check(name, t, None, (S, H, V, K), cuda)
+    return B, T, H, K, V, N
+
+
+def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+        initial_state=None, final_state=None, cu_seqlens=None):
+    """Chunked KDA forward on the current CUDA stream. Writes ``out`` (and
+    ``final_state`` if given) in place and returns ``(out, final_state)``."""
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=True)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                          _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                          _ptr(initial_state), _state_code(initial_state),
+                          _ptr(final_state), _state_code(final_state),
+                          _ptr(cu_seqlens), N, B, T, H, K, V, ctypes.c_void_p(stream))
+    _raise(st)
+    return out, final_state
+
+
+def fwd_host(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+             initial_state=None, final_state=None, cu_seqlens=None, device=None):
+    """Same operation on CPU tensors (pin them for fast copies): the library
+    copies inputs to the GPU, runs, copies ``out``/``final_state`` back and
+    synchronises before returning."""
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=False)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = _lib.kda_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                               _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                               _ptr(initial_state), _state_code(initial_state),
+                               _ptr(final_state), _state_code(final_state),
+                               _ptr(cu_seqlens), N, B, T, H, K, V, ctypes.c_void_p(stream))
+    _raise(st)
+    return out, final_state
+
+
+def check_device_status(stream=None):
+    """Synchronise ``stream`` and raise if the kernels flagged a device-side error."""
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    _raise(_lib.kda_check_device_status(ctypes.c_void_p(s)))
+
+
+def gate_scale(lower_bound: float) -> float:
+    return _lib.kda_gate_scale(float(lower_bound))
+
+
+def plan(units: int, num_sms: int):
+    vs, grid = _I(), _I64()
+    _raise(_lib.kda_plan(int(units), int(num_sms), ctypes.byref(vs), ctypes.byref(grid)))
+    return vs.value, grid.value
+
+
+def version() -> int:
+    return _lib.kda_version()
+
+
+def library():
+    """The loaded ctypes handle of libkda.so (for direct C-ABI calls)."""
+    return _lib

@@ -1,0 +1,170 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) chunked forward pass for
+ * GB300 (sm_103a). One shared library, libkda.so; plain pointers and sizes,
+ * no framework types.
+ *
+ * The operation. For every sequence and head, with state S (V x K, stored
+ * row-major [v][k]) and per token t:
+ *
+ *   a_t[c]  = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h,c]))
+ *             (A_log NULL: factor 1; dt_bias NULL: bias 0)
+ *   beta_t  = sigmoid(beta logit_t)
+ *   S_t     = S_{t-1} Diag(exp(a_t)) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   out_t   = scale * S_t q_t
+ *
+ * Sources (page title -- section):
+ *  [LB]     "FlashKDA lower_bound Parameter: Controlling Exponentiation
+ *           Precision in Selective State Space Models": "Conversion to the
+ *           Gate Scale Factor" (gate_scale = lower_bound * log2(e)), "How does
+ *           lower_bound interact with dt_bias?" (the gate), "Can lower_bound
+ *           be positive?".
+ *  [EX2]    "Base-2 Exponent Optimization in FlashKDA: How It Works and
+ *           Performance Benefits": "Re-basing the Gate Activation".
+ *  [CHUNK]  "How FlashKDA's CHUNK Size of 16 Improves Numerical Stability
+ *           Over CHUNK 64": "Efficient 16x16 Matrix Inversion" (16-token
+ *           chunks, the unit-lower chunk matrix and its inverse).
+ *  [SHAPES] "FlashKDA Input Tensor Shapes and DTypes: Complete Specification
+ *           for the Forward Pass": "Query, Key, and Value Tensors", "Gating
+ *           Tensors and Output Buffer", "Global Scaling Factor", "Gating
+ *           Parameters and Constraints", "Initial and Final States",
+ *           "Variable-Length Mode", "Memory Layout and Hardware Requirements".
+ * The pages name the method but do not print the state update; the update
+ * above is the gated delta rule with a per-channel decay, the published
+ * definition of KDA. How A_log enters the gate is not stated on the pages;
+ * exp(A_log[h]) multiplying the biased gate is the reading adopted here.
+ *
+ * Ownership and execution. The caller owns every buffer; all pointers below
+ * are DEVICE pointers except where noted. kda_fwd allocates no device memory,
+ * keeps no per-call state, never synchronises, and runs asynchronously on the
+ * caller's stream. Inputs are never modified. `out` is written in place
+ * [SHAPES "Gating Tensors and Output Buffer"].
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Status codes. Every entry point returns one; nothing aborts the process. */
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,            /* a required pointer is NULL */
+    KDA_ERR_SHAPE = 2,           /* K or V != 128, B/T/H/N out of range, varlen with B != 1 */
+    KDA_ERR_DTYPE = 3,           /* unsupported state dtype code */
+    KDA_ERR_RANGE = 4,           /* lower_bound outside [-5, 0] or not finite; scale not finite */
+    KDA_ERR_STATE_MISMATCH = 5,  /* initial/final state dtypes differ, or buffers overlap partially */
+    KDA_ERR_ALIGN = 6,           /* a pointer is not aligned as required */
+    KDA_ERR_LAUNCH = 7,          /* a CUDA call failed; see kda_last_error() */
+    KDA_ERR_DEVICE = 8           /* the device reported an error (kda_check_device_status) */
+} kda_status;
+
+/* Element type of the optional recurrent states [SHAPES "Initial and Final States"]. */
+typedef enum kda_dtype {
+    KDA_DTYPE_NONE = 0,          /* buffer absent (pointer must be NULL) */
+    KDA_DTYPE_BF16 = 1,
+    KDA_DTYPE_FP32 = 2
+} kda_dtype;
+
+/*
+ * kda_fwd -- the chunked KDA forward pass (CHUNK = 16 [CHUNK]).
+ *
+ * Tensors (all row-major, contiguous, DEVICE memory):
+ *   q, k, g   bf16  [B, T, H, K]        queries, keys, gate pre-activations (16-byte aligned)
+ *   v         bf16  [B, T, H, V]        values (16-byte aligned)
+ *   beta      bf16  [B, T, H]           beta logits (sigmoid applied inside)
+ *   out       bf16  [B, T, H, V]        written for every token (16-byte aligned)
+ *   A_log     fp32  [H]     or NULL     per-head log gate parameter
+ *   dt_bias   fp32  [H, K]  or NULL     gate bias
+ *   initial_state  [S, H, V, K] or NULL, dtype initial_dtype (S = B, or N)
+ *   final_state    [S, H, V, K] or NULL, dtype final_dtype; receives the
+ *                  state after each sequence's last token. It may be the
+ *                  same buffer as initial_state (in-place update); partial
+ *                  overlap is rejected. States are 16-byte aligned.
+ *   cu_seqlens int64 [N+1] or NULL      varlen mode: B must be 1, T is the
+ *                  packed length, sequence i spans tokens
+ *                  [cu_seqlens[i], cu_seqlens[i+1]) [SHAPES "Variable-Length
+ *                  Mode"]. Entries are read on the device only; a sequence
+ *                  outside [0, T] or with a decreasing bound is skipped and
+ *                  flags KDA_ERR_DEVICE for kda_check_device_status().
+ * Scalars:
+ *   scale        multiplies the output [SHAPES "Global Scaling Factor"].
+ *   lower_bound  must lie in [-5, 0] [SHAPES "Gating Parameters and
+ *                Constraints"]; the kernel uses gate_scale = lower_bound *
+ *                log2(e) with base-2 exponentials [LB, EX2].
+ *   B, T, H      batch, tokens per batch row (packed length in varlen), heads.
+ *   K, V         head dimensions; both must be 128 [SHAPES "Memory Layout
+ *                and Hardware Requirements"].
+ *   N            number of sequences in varlen mode (>= 1); ignored otherwise.
+ *   stream       a cudaStream_t (NULL = legacy default stream).
+ * A state absent from the call is zero (initial) or not written (final).
+ * Returns KDA_OK once the work is enqueued. Argument errors are detected on
+ * the host before anything is launched and leave every buffer untouched.
+ */
+KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, float scale, void *out,
+                           const float *A_log, const float *dt_bias, float lower_bound,
+                           const void *initial_state, kda_dtype initial_dtype,
+                           void *final_state, kda_dtype final_dtype,
+                           const int64_t *cu_seqlens, int64_t N,
+                           int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                           void *stream);
+
+/*
+ * kda_fwd_host -- the same operation on HOST buffers (same layouts and
+ * arguments as kda_fwd, every pointer a host pointer; pinned memory gives
+ * the fastest copies). It stages the inputs in stream-ordered device memory
+ * that it allocates for the call, runs kda_fwd on `stream`, copies `out` and
+ * `final_state` back, frees the staging memory and synchronises `stream`
+ * before it returns. This is the end-to-end entry point for callers whose
+ * tensors live in host memory.
+ */
+KDA_API kda_status kda_fwd_host(const void *q, const void *k, const void *v, const void *g,
+                                const void *beta, float scale, void *out,
+                                const float *A_log, const float *dt_bias, float lower_bound,
+                                const void *initial_state, kda_dtype initial_dtype,
+                                void *final_state, kda_dtype final_dtype,
+                                const int64_t *cu_seqlens, int64_t N,
+                                int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                                void *stream);
+
+/* gate_scale = lower_bound * log2(e), rounded to float, exactly as the kernel
+ * receives it [LB "Conversion to the Gate Scale Factor"]. Host only. */
+KDA_API float kda_gate_scale(float lower_bound);
+
+/*
+ * kda_plan -- the launch plan kda_fwd would use (host only, no GPU needed):
+ * for `units` independent (sequence, head) pairs on a device with `num_sms`
+ * multiprocessors, writes the number of CTAs each state's V rows are split
+ * across (1, 2, 4 or 8) and the grid size. Returns KDA_ERR_NULL for NULL
+ * outputs and KDA_ERR_SHAPE for units < 0 or num_sms < 1.
+ */
+KDA_API kda_status kda_plan(int64_t units, int num_sms, int *v_split, int64_t *grid);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+KDA_API const char *kda_last_error(void);
+
+/*
+ * kda_check_device_status -- synchronises `stream`, then reads and clears the
+ * library's device error word (bad cu_seqlens entries, or a pipeline wait
+ * that hit its iteration limit). Returns KDA_OK, KDA_ERR_DEVICE (details in
+ * kda_last_error()) or KDA_ERR_LAUNCH.
+ */
+KDA_API kda_status kda_check_device_status(void *stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from gated_linear_attention_kda_gb300 import _build
+    _build.build_library()
+    import gated_linear_attention_kda_gb300 as m
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    assert {"kda_fwd", "kda_fwd_host", "kda_check_device_status", "kda_last_error", "kda_plan",
+            "kda_gate_scale", "kda_version"} <= set(syms)
+
+
+def test_library_exports_every_declared_symbol(kda):
+    lib = ctypes.CDLL(kda.LIB_PATH)
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"libkda.so does not export {s}"
+
+
+def test_gate_scale_matches_the_page_constant(kda):
+    # gate_scale = float(lower_bound * 1.4426950408889634): "Conversion to the Gate Scale Factor"
+    import numpy as np
+    for lb in (-5.0, -2.0, -0.5, 0.0):
+        assert kda.gate_scale(lb) == np.float32(lb * 1.4426950408889634)
+
+
+def test_plan_fills_the_machine(kda):
+    assert kda.plan(128, 152) == (1, 128)     # one CTA per state
+    assert kda.plan(32, 152) == (4, 128)      # V rows split four ways
+    assert kda.plan(16, 152) == (8, 128)
+    assert kda.plan(1, 152) == (8, 8)
+    assert kda.plan(512, 152) == (1, 512)
+    assert kda.plan(0, 152) == (8, 0)
+    with pytest.raises(ValueError):
+        kda.plan(-1, 152)
+    with pytest.raises(ValueError):
+        kda.plan(4, 0)
+
+
+def _call(kda, **over):
+    """Direct C-ABI call with dummy (never dereferenced) aligned pointers."""
+    args = dict(q=0x1000, k=0x2000, v=0x3000, g=0x4000, beta=0x5000, scale=1.0, out=0x6000, A_log=None,
+                dt_bias=None, lb=-5.0, init=None, init_dt=0, fin=None, fin_dt=0, cu=None, N=0,
+                B=1, T=16, H=1, K=128, V=128, stream=None)
+    args.update(over)
+    lib = kda.library()
+    return lib.kda_fwd(*[args[x] for x in ("q", "k", "v", "g", "beta", "scale", "out", "A_log", "dt_bias", "lb",
+                                           "init", "init_dt", "fin", "fin_dt", "cu", "N", "B", "T", "H", "K",
+                                           "V", "stream")])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), 2), (dict(V=256), 2), (dict(H=0), 2), (dict(B=0), 2), (dict(T=-1), 2),
+    (dict(cu=0x7000, B=2, N=1), 2), (dict(cu=0x7000, N=0), 2),
+    (dict(q=None), 1), (dict(beta=None), 1), (dict(out=None), 1),
+    (dict(lb=-5.5), 4), (dict(lb=0.25), 4), (dict(lb=float("nan")), 4), (dict(scale=float("inf")), 4),
+    (dict(init=0x8000, init_dt=0), 3), (dict(init=None, init_dt=1), 3), (dict(fin=0x8000, fin_dt=7), 3),
+    (dict(init=0x8000, init_dt=1, fin=0x9000000, fin_dt=2), 5),
+    (dict(init=0x100000, init_dt=2, fin=0x100000 + 4096, fin_dt=2), 5),
+    (dict(q=0x1008), 6), (dict(out=0x6002), 6), (dict(beta=0x5001), 6),
+    (dict(init=0x8008, init_dt=2), 6), (dict(cu=0x7004, N=1), 6),
+])
+def test_host_validation_rejects(kda, over, code):
+    assert _call(kda, **over) == code
+    assert kda.library().kda_last_error()
+
+
+def test_python_wrapper_rejects_bad_tensors(kda):
+    import torch
+    q = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16)
+    beta = torch.zeros(1, 16, 1, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.fwd(q, q, q, q, beta, 1.0, q.clone())
+    with pytest.raises(ValueError, match="CPU tensor|contiguous|bfloat16|shape"):
+        kda.fwd_host(q, q, q, q, beta.float(), 1.0, q.clone())
+    with pytest.raises(ValueError, match="contiguous"):
+        qt = torch.zeros(1, 16, 1, 256, dtype=torch.bfloat16)[..., :128]
+        kda.fwd_host(qt, q, q, q, beta, 1.0, q.clone())

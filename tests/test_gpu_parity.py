@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded
+inputs, element by element, with the stated tolerance (relative L2 <= 5e-3,
+|err| <= 2e-2 + 2e-2 |ref|) on ``out`` and ``final_state``."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.kda_harness import assert_close, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(d, final_dtype="fp32", heads=None, **kw):
+    o, s = run_gpu(d, final_dtype=final_dtype, **kw)
+    o_ref, s_ref = run_oracle(d, heads=heads, lower_bound=kw.get("lower_bound"), scale=kw.get("scale"))
+    if heads is not None:
+        o, s = o[:, :, heads], (None if s is None else s[:, heads])
+    rel = assert_close("out", o, o_ref)
+    if s is not None:
+        assert_close("final_state", s, s_ref)
+    return rel
+
+
+def test_small_one_head_four_chunks():
+    _check(W.make("b1_t64_h1"))
+
+
+def test_state_carry_case_fp32_states():
+    _check(W.make("b2_t128_h8"))
+
+
+def test_split_call_equals_one_call():
+    """T = 128 as 64 + 64 through final_state -> initial_state."""
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8")
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    half = lambda x, a, b: x[:, a:b].contiguous()
+    out1 = torch.empty_like(half(c["v"], 0, 64))
+    out2 = torch.empty_like(out1)
+    mid = torch.empty_like(c["initial_state"])
+    fin = torch.empty_like(c["initial_state"])
+    args = lambda a, b: [half(c[x], a, b) for x in ("q", "k", "v", "g", "beta")]
+    kda.fwd(*args(0, 64), d["scale"], out1, c["A_log"], c["dt_bias"], d["lower_bound"], c["initial_state"], mid)
+    kda.fwd(*args(64, 128), d["scale"], out2, c["A_log"], c["dt_bias"], d["lower_bound"], mid, fin)
+    kda.check_device_status()
+    o_ref, s_ref = run_oracle(d)
+    assert_close("out", torch.cat([out1, out2], 1).float().cpu().double().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().double().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("T", [1, 15, 17, 37, 100])
+def test_ragged_lengths(T):
+    _check(W.make("b2_t128_h8", T=T, H=3))
+
+
+@pytest.mark.parametrize("lb", [0.0, -0.5, -5.0])
+def test_lower_bound_range(lb):
+    _check(W.make("b2_t128_h8", B=1, H=4), lower_bound=lb)
+
+
+def test_no_gate_parameters_bf16_states():
+    d = W.make("b8_t4096_h16", B=2, T=200, H=5)
+    d["initial_state"] = (torch.randn(2, 5, 128, 128, generator=torch.Generator().manual_seed(9)) * 0.02).to(torch.bfloat16)
+    _check(d, final_dtype="bf16")
+
+
+def test_in_place_state_equals_out_of_place():
+    d = W.make("b2_t128_h8", T=77)
+    o1, s1 = run_gpu(d)
+    o2, s2 = run_gpu(d, in_place=True)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_deterministic_repeats():
+    d = W.make("b2_t128_h8", T=99, H=4)
+    a = run_gpu(d)
+    b = run_gpu(d)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_no_final_state_and_zero_scale():
+    d = W.make("b1_t64_h1")
+    o, s = run_gpu(d, final_dtype=None, scale=0.0)
+    assert s is None and np.all(o == 0)
+
+
+def test_varlen_small_with_empty_and_ragged_sequences():
+    d = W.make("varlen_n16_h32", lengths=[5, 37, 16, 1, 0, 23, 64, 40], H=3)
+    _check(d, final_dtype="bf16")
+
+
+def test_varlen_equals_separate_calls():
+    lens = [19, 48, 3, 33]
+    d = W.make("varlen_n16_h32", lengths=lens, H=2)
+    o, s = run_gpu(d, final_dtype="bf16")
+    cu = d["cu_seqlens"]
+    for i in range(len(lens)):
+        a, b = int(cu[i]), int(cu[i + 1])
+        di = dict(d)
+        for k in ("q", "k", "v", "g", "beta"):
+            di[k] = d[k][:, a:b].contiguous()
+        di["initial_state"] = d["initial_state"][i:i + 1].contiguous()
+        di["cu_seqlens"] = None
+        oi, si = run_gpu(di, final_dtype="bf16")
+        assert np.array_equal(oi, o[:, a:b]) and np.array_equal(si[0], s[i])
+
+
+def test_bad_cu_seqlens_flags_device_error_without_fault():
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("varlen_n16_h32", lengths=[50, 10, 40], H=2)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    c["cu_seqlens"] = torch.tensor([0, 50, 30, 100], dtype=torch.int64, device="cuda")  # decreasing bound
+    out = torch.zeros_like(c["v"])
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], None, c["cu_seqlens"])
+    with pytest.raises(kda.KDAError, match="KDA_ERR_DEVICE"):
+        kda.check_device_status()
+    kda.check_device_status()  # the word is cleared after it was reported
+    torch.cuda.synchronize()   # the context is still healthy
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", T=45)
+    o_dev, s_dev = run_gpu(d)
+    out = torch.empty_like(d["v"]).pin_memory()
+    fin = torch.empty_like(d["initial_state"]).pin_memory()
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], d["scale"], out, pin["A_log"],
+                 pin["dt_bias"], d["lower_bound"], pin["initial_state"], fin)
+    assert np.array_equal(out.float().double().numpy(), o_dev)
+    assert np.array_equal(fin.double().numpy(), s_dev)
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def test_full_b8_t4096_h16_sampled_heads():
+    """The throughput workload at full size, in the launch configuration the
+    benchmark times; the oracle checks every token of three sampled heads."""
+    d = W.make("b8_t4096_h16")
+    _check(d, heads=[0, 7, 15])
+
+
+def test_full_varlen_n16_h32_sampled_heads():
+    d = W.make("varlen_n16_h32")
+    _check(d, final_dtype="bf16", heads=[0, 31])
+
+
+def test_full_long_context_sampled_head():
+    d = W.make("b1_t131072_h32")
+    _check(d, heads=[5])
