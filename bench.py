@@ -1,0 +1,333 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA chunked forward pass on GB300.
+
+One step = one ``kda_fwd`` call over the whole B=8, T=4096, H=16, K=V=128
+workload (lower_bound -5, no gate parameters, fp32 final state), inputs
+resident in HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step). Under torchrun (N > 1) each
+rank runs its own copy of the workload on its GPU (weak scaling, no
+collective on the data path); the reference arm runs on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd tokens/s at B=8,T=4096,H=16; achieved HBM GB/s & % of roofline"
+UNIT = "tokens/s"
+WORKLOAD = "b8_t4096_h16"
+BYTES_PER_TOKEN_HEAD = 4 * 256 + 2 + 256     # q, k, v, g in; beta in; out
+FLOPS_PER_CHUNK_HEAD = 3 * 2 * 16 * 128 * 128 + 5 * 2 * 16 * 16 * 128 + 2 * 16 ** 3
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+KERNEL_SOURCES = ["gated_linear_attention_kda_gb300/csrc/kda_fwd.cu", "gated_linear_attention_kda_gb300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_kernel.b8_t4096_h16.traffic.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def algorithmic(w, d):
+    B, T, H = d["q"].shape[0], d["q"].shape[1], d["q"].shape[2]
+    nseq = B if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    st = nseq * H * 128 * 128
+    state_bytes = (st * d["initial_state"].element_size() if d["initial_state"] is not None else 0) + st * 4
+    nbytes = BYTES_PER_TOKEN_HEAD * B * T * H + state_bytes
+    chunks = B * H * math.ceil(T / 16)
+    return nbytes, chunks * FLOPS_PER_CHUNK_HEAD
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self):
+        return time.perf_counter()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if t0 - 0.06 <= t <= t1 + 0.06] or [l for (_, l) in self.lines[-3:]]
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_time(d, nthreads, batch_rows):
+    """Time the fp64 oracle on the first ``batch_rows`` rows of the workload."""
+    import oracle
+    import workloads as W
+    sl = lambda x: x[:batch_rows].contiguous()
+    bits = {k: W.bf16_bits(sl(d[k])) for k in ("q", "k", "v", "g", "beta")}
+    A = None if d["A_log"] is None else d["A_log"].numpy()
+    db = None if d["dt_bias"] is None else d["dt_bias"].numpy()
+    init = None if d["initial_state"] is None else W.state_f64(sl(d["initial_state"]))
+    t0 = time.perf_counter()
+    oracle.fwd(bits["q"], bits["k"], bits["v"], bits["g"], bits["beta"], d["scale"], A, db, d["lower_bound"],
+               init, None, nthreads=nthreads)
+    return time.perf_counter() - t0, batch_rows * d["q"].shape[1]
+
+
+def cpu_baseline(d):
+    import oracle
+    oracle.build()
+    n = oracle.default_threads()
+    B = d["q"].shape[0]
+    secs, toks = oracle_time(d, n, 1)
+    rows = max(1, min(B, int(10.0 / max(secs, 1e-3))))   # aim at ~10 s of CPU work
+    if rows > 1:
+        secs, toks = oracle_time(d, n, rows)
+    return {"value": toks / secs, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{rows} of {B} batch rows x {d['q'].shape[1]} tokens x {d['q'].shape[2]} heads, "
+                      f"fp64 per-token recurrence, {secs:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+    oracle.build()
+    d = W.make(WORKLOAD)
+    n = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle_time(d, n, 1)
+    total_s, total_tok = 0.0, 0
+    for _ in range(args.steps):
+        s, t = oracle_time(d, n, 1)
+        total_s += s
+        total_tok += t
+    v = total_tok / total_s
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD, "B": 8, "T": 4096, "H": 16, "K": 128, "V": 128,
+                       "sample_per_step": "1 of 8 batch rows (4096 tokens x 16 heads)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": n, "kind": "oracle",
+                             "sample": "1 of 8 batch rows x 4096 tokens x 16 heads per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import gated_linear_attention_kda_gb300 as kda
+    import workloads as W
+
+    d = W.make(WORKLOAD)
+    B, T, H = d["q"].shape[0], d["q"].shape[1], d["q"].shape[2]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    c = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    fin = torch.empty(B, H, 128, 128, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    kda.check_device_status()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter()
+    barrier(world)
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    clocks = sampler.stop(t_start, t_end) if rank == 0 else None
+    kda.check_device_status()
+
+    # end to end through the host-buffer entry point: H2D inputs, kernel, D2H result, every step
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    hout = torch.empty_like(d["v"]).pin_memory()
+    hfin = torch.empty(B, H, 128, 128, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], d["scale"], hout, pin["A_log"],
+                     pin["dt_bias"], d["lower_bound"], pin["initial_state"], hfin, pin["cu_seqlens"], device=dev)
+
+    e2e_steps = max(1, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "g", "beta"))
+    d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+
+    if rank != 0:
+        return
+    tokens = B * T
+    ms_per_step = elapsed_ms / args.steps
+    value = world * tokens * args.steps / (elapsed_ms / 1e3)
+    nbytes, nflops = algorithmic(WORKLOAD, d)
+    hbm, tflops, src = peaks()
+    achieved = nbytes / (ms_per_step / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_hash") == kernel_hash():
+            traffic = tr["bytes_per_launch"]
+    except Exception:
+        pass
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "K": 128, "V": 128, "lower_bound": -5.0,
+                   "gate_params": False, "final_state": "fp32",
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.1f} MB per step, no flush)",
+                   "parallelism": f"{world} independent replica(s), one CTA per (sequence, head) state"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": src, "algorithmic_bytes_per_launch": nbytes,
+                     "tensor_frac": (nflops / (ms_per_step / 1e3) / 1e12) / tflops},
+        "cpu_baseline": cpu_baseline(d) if world == 1 or rank == 0 else None,
+        "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        "libkda.so is not built; run `python -m gated_linear_attention_kda_gb300._build` "
+        "libkda.so is not built; run `python gated_linear_attention_kda_gb300/_build.py` "
         "(or __graft_entry__.build()) first")
 
 _lib = ctypes.CDLL(LIB_PATH)

@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "kda.h")
 
 @pytest.fixture(scope="module")
 def kda():
-    from gated_linear_attention_kda_gb300 import _build
-    _build.build_library()
+    import __graft_entry__
+    __graft_entry__._builder().build_library()
     import gated_linear_attention_kda_gb300 as m
     return m
 
