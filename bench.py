@@ -309,13 +309,35 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_launches(n):
+    """Run ``n`` forward passes of the benchmark workload (for profilers)."""
+    import torch
+
+    import gated_linear_attention_kda_gb300 as kda
+    import workloads as W
+    d = W.make(WORKLOAD)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    fin = torch.empty(d["q"].shape[0], d["q"].shape[2], 128, 128, dtype=torch.float32, device="cuda")
+    for _ in range(n):
+        kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+    kda.check_device_status()
+    print(f"ran {n} launches of {WORKLOAD}")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--launches", type=int, default=0,
+                    help="profiling mode: run this many forward passes of the workload and exit (no timing)")
     args = ap.parse_args()
+    if args.launches:
+        run_launches(args.launches)
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)
