@@ -1,0 +1,100 @@
+// kda_common.cuh -- definitions shared by the KDA forward kernels: launch
+// parameters, the device error word, bounded mbarrier waits and the layout of
+// the TMA-loaded q/k/v/g chunk tiles.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kda.h"
+#include "ptx.cuh"
+
+namespace kda {
+
+constexpr int CHUNK = 16;
+constexpr int DH = 128;  // K = V = 128
+constexpr int RAW_TILE = 4096;        // 16 rows x 128 bf16, as two 64-column TMA boxes
+constexpr int RAW_BOX = 2048;
+constexpr int RAW_STAGE = 4 * RAW_TILE;
+constexpr int OFF_Q = 0, OFF_K = RAW_TILE, OFF_V = 2 * RAW_TILE, OFF_G = 3 * RAW_TILE;
+
+constexpr float LOG2E = 1.4426950408889634f;
+// tf32 operands are taken from fp32 bit patterns (low mantissa bits ignored).
+// Scaling by 1 + 2^-11 first centres that truncation error on zero.
+constexpr float TRUNC_COMP = 1.00048828125f;
+
+constexpr int SPIN_LIMIT = 1 << 22;
+
+enum : unsigned { DEVERR_SEQLENS = 1u, DEVERR_TIMEOUT = 2u };
+__device__ unsigned int g_dev_error;
+
+struct Params {
+    const uint16_t *beta;
+    uint16_t *out;
+    const float *A_log;
+    const float *dt_bias;
+    const void *init;
+    void *fin;
+    const int64_t *cu;
+    int init_dtype, fin_dtype;
+    int T;        // tokens per batch row (batched mode)
+    int H;
+    int nseq;     // B, or N in varlen mode
+    int vsplit;   // CTAs per state
+    int total;    // length of the flattened token axis (B * T)
+    float scale;
+    float half_gs;  // 0.5 * lower_bound * log2(e)
+};
+
+// Bounded wait on an mbarrier phase. Gives up when another role has already
+// given up (abort flag) or after SPIN_LIMIT polls, which flags the device
+// error word; the caller then leaves its loop so the CTA always terminates.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+#pragma unroll 1
+    for (int i = 0; i < SPIN_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    atomicOr(&g_dev_error, DEVERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
+{
+#pragma unroll 1
+    for (int i = 0; i < SPIN_LIMIT; ++i)
+        if (mbar_try_wait(bar, parity)) return;
+    atomicOr(&g_dev_error, DEVERR_TIMEOUT);
+}
+
+struct Span {
+    int bos, len;
+    bool ok;
+};
+
+__device__ __forceinline__ Span seq_span(const Params &p, int seq)
+{
+    if (p.cu) {
+        const long long b = p.cu[seq], e = p.cu[seq + 1];
+        if (b < 0 || e < b || e > p.total) return {0, 0, false};
+        return {static_cast<int>(b), static_cast<int>(e - b), true};
+    }
+    return {seq * p.T, p.T, true};
+}
+
+// Byte offset of element (row r, channel c) inside a 16x128 bf16 tile loaded
+// as two 64-column boxes with the 128-byte swizzle (16-byte chunk index XOR
+// row mod 8).
+__device__ __forceinline__ uint32_t raw_off(int r, int c)
+{
+    return (c >> 6) * RAW_BOX + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2;
+}
+
+__device__ __forceinline__ uint16_t f2bf_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ uint16_t f2h_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+
+}  // namespace kda

@@ -1,0 +1,391 @@
+// kda_fwd_mma.cuh -- the KDA forward kernel with warp-level MMA state
+// products (state rows in registers). Used when a state's V rows are split
+// across several CTAs (few states); see kda_fwd_tc.cuh for the tcgen05 kernel.
+#pragma once
+#include "kda_common.cuh"
+
+namespace kda {
+namespace v1 {
+
+// ---------------------------------------------------------------- shared memory plan
+constexpr int NR = 6;                 // raw q/k/v/g ring depth (chunks)
+constexpr int NP = 2;                 // prep ring depth = number of prep lanes
+
+constexpr int BZ_LD = 272;            // row pitch (bytes) of 128-wide 16-bit tiles (136 elements)
+constexpr int SM_LD = 48;             // row pitch of 16x16 16-bit tiles (24 elements)
+constexpr int P_BZ = 0;                           // bf16 [32][136]: K*Gamma rows 0-15, Q*Gamma rows 16-31
+constexpr int P_KB = P_BZ + 32 * BZ_LD;           // f16  [16][136]: Kbar
+constexpr int P_TT = P_KB + 16 * BZ_LD;           // f16  [16][24]:  T diag(beta)
+constexpr int P_PP = P_TT + 16 * SM_LD;           // f16  [16][24]:  P
+constexpr int P_GAM = P_PP + 16 * SM_LD;          // f32  [128]:     gamma = Gamma at chunk end
+constexpr int PREP_SLOT = P_GAM + DH * 4;
+
+constexpr int F_LD = 528;             // row pitch of fp32 [16][132] tiles
+constexpr int A_LD = 80;              // row pitch of fp32 [16][20] tiles
+constexpr int S_KL = 0;               // tf32 K * 2^(G - G_mid)
+constexpr int S_QL = 16 * F_LD;       // tf32 Q * 2^(G - G_mid)
+constexpr int S_KR = 32 * F_LD;       // tf32 K * 2^(G_mid - G)
+constexpr int S_AM = 48 * F_LD;       // fp32 A
+constexpr int S_BETA = S_AM + 16 * A_LD;
+constexpr int SCR = S_BETA + 64;
+
+constexpr int OFF_RAW = 0;
+constexpr int OFF_PREP = OFF_RAW + NR * RAW_STAGE;
+constexpr int OFF_SCR = OFF_PREP + NP * PREP_SLOT;
+constexpr int OFF_BAR = OFF_SCR + NP * SCR;
+constexpr int NBAR = 2 * NR + 2 * NP;
+constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;
+constexpr int SMEM_USED = OFF_FLAGS + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // the ring base is rounded up to 1024 B (128B swizzle)
+
+static_assert(PREP_SLOT % 16 == 0 && SCR % 16 == 0 && OFF_PREP % 1024 == 0, "alignment");
+static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+
+template <int NS>
+__global__ void __launch_bounds__(32 * (5 + NS), 1)
+    kda_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
+{
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int unit = blockIdx.x / p.vsplit, slice = blockIdx.x % p.vsplit;
+    const int seq = unit / p.H, h = unit % p.H;
+    const Span sp = seq_span(p, seq);
+
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
+    const uint32_t raw_full = sb + OFF_BAR, raw_empty = raw_full + NR * 8;
+    const uint32_t prep_full = raw_empty + NR * 8, prep_empty = prep_full + NP * 8;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(raw_full + 8 * i, 1);
+            mbar_init(raw_empty + 8 * i, 1 + NS);
+        }
+        for (int i = 0; i < NP; ++i) {
+            mbar_init(prep_full + 8 * i, 1);
+            mbar_init(prep_empty + 8 * i, NS);
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+        if (p.cu && blockIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.nseq] != p.total))
+            atomicOr(&g_dev_error, DEVERR_SEQLENS);
+        if (!sp.ok && slice == 0 && h == 0) atomicOr(&g_dev_error, DEVERR_SEQLENS);
+    }
+    __syncthreads();
+    if (!sp.ok) return;  // CTA-uniform
+    const int nch = (sp.len + CHUNK - 1) / CHUNK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tg);
+            int n = 0;
+            for (; n < nch; ++n) {
+                const int s = n % NR;
+                const uint32_t ph = (n / NR) & 1;
+                if (!wait_bar(raw_empty + 8 * s, ph ^ 1, flags)) break;
+                const uint32_t fb = raw_full + 8 * s;
+                mbar_arrive_expect_tx(fb, RAW_STAGE);
+                const int tok = sp.bos + n * CHUNK;
+                const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(dst + OFF_Q + b * RAW_BOX, &tq, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_K + b * RAW_BOX, &tk, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_V + b * RAW_BOX, &tv, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_G + b * RAW_BOX, &tg, 64 * b, h, tok, fb);
+                }
+            }
+            // never leave while copies this thread issued may still be landing
+            for (int m = (n > NR ? n - NR : 0); m < n; ++m) drain_bar(raw_full + 8 * (m % NR), (m / NR) & 1);
+        }
+        return;
+    }
+
+    if (warp < 5) {
+        // ------------------------------------------------------------ prep lanes
+        const int ln = (warp - 1) >> 1;            // prep lane 0 or 1
+        const int lt = threadIdx.x - 32 - 64 * ln;  // 0..63
+        const int lw = lt >> 5;                     // warp within the lane
+        const uint32_t bar_id = 1 + ln;
+        const uint32_t scr = sb + OFF_SCR + ln * SCR;
+        const uint32_t pslot = sb + OFF_PREP + ln * PREP_SLOT;
+        const int c0 = 2 * lt;                      // this thread's channels c0, c0 + 1
+        float a_h = 1.f, bias0 = 0.f, bias1 = 0.f;
+        if (p.A_log) a_h = ex2_approx(__ldg(p.A_log + h) * LOG2E);
+        if (p.dt_bias) {
+            bias0 = __ldg(p.dt_bias + h * DH + c0);
+            bias1 = __ldg(p.dt_bias + h * DH + c0 + 1);
+        }
+        const float hs = p.half_gs;
+        const int g = lane >> 2, t = lane & 3;
+
+        for (int n = ln; n < nch; n += NP) {
+            bool failed = false;  // this thread's waits gave up; OR-reduced at the end of the chunk
+            const int rs = n % NR;
+            const uint32_t rph = (n / NR) & 1, pph = (n / NP) & 1;
+            const int tok0 = sp.bos + n * CHUNK;
+            const int Lv = min(CHUNK, sp.len - n * CHUNK);
+            float blogit = 0.f;
+            if (lw == 1 && lane < Lv)
+                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lane) * p.H + h)) << 16);
+            if (!wait_bar(raw_full + 8 * rs, rph, flags)) failed = true;
+            const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
+
+            // gate in log2 units and its inclusive in-chunk cumsum
+            float G0[CHUNK], G1[CHUNK];
+            {
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int r = 0; r < CHUNK; ++r) {
+                    const uint32_t gw = lds32(raw + OFF_G + raw_off(r, c0));
+                    const float x0 = a_h * (bf16_lo(gw) + bias0), x1 = a_h * (bf16_hi(gw) + bias1);
+                    // gate_scale * sigmoid(x) = hs + hs * tanh(x / 2)
+                    const float ga0 = fmaf(hs, tanh_approx(0.5f * x0), hs);
+                    const float ga1 = fmaf(hs, tanh_approx(0.5f * x1), hs);
+                    acc0 += (r < Lv) ? ga0 : 0.f;
+                    acc1 += (r < Lv) ? ga1 : 0.f;
+                    G0[r] = acc0;
+                    G1[r] = acc1;
+                }
+            }
+            if (!wait_bar(prep_empty + 8 * ln, pph ^ 1, flags)) failed = true;
+
+            const float Gm0 = G0[7], Gm1 = G1[7];  // mid-chunk reference halves the exponent range
+            const float sm0 = ex2_approx(-Gm0) * TRUNC_COMP, sm1 = ex2_approx(-Gm1) * TRUNC_COMP;
+            const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
+            stsf2(pslot + P_GAM + c0 * 4, ex2_approx(G0[15]), ex2_approx(G1[15]));
+#pragma unroll
+            for (int r = 0; r < CHUNK; ++r) {
+                const uint32_t kw = lds32(raw + OFF_K + raw_off(r, c0));
+                const uint32_t qw = lds32(raw + OFF_Q + raw_off(r, c0));
+                const bool live = r < Lv;
+                const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
+                const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
+                const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);            // Gamma_r
+                const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);  // 2^(G_mid - G_r)
+                sts32(pslot + P_BZ + r * BZ_LD + c0 * 2, pack_bf16(k0 * gm0, k1 * gm1));
+                sts32(pslot + P_BZ + (16 + r) * BZ_LD + c0 * 2, pack_bf16(q0 * gm0, q1 * gm1));
+                sts32(pslot + P_KB + r * BZ_LD + c0 * 2, pack_f16(k0 * f0 * se0, k1 * f1 * se1));
+                const float u0 = gm0 * sm0, u1 = gm1 * sm1;                              // 2^(G_r - G_mid)
+                stsf2(scr + S_KL + r * F_LD + c0 * 4, k0 * u0, k1 * u1);
+                stsf2(scr + S_QL + r * F_LD + c0 * 4, q0 * u0, q1 * u1);
+                stsf2(scr + S_KR + r * F_LD + c0 * 4, k0 * f0 * TRUNC_COMP, k1 * f1 * TRUNC_COMP);
+            }
+            if (lw == 1 && lane < CHUNK)
+                stsf(scr + S_BETA + lane * 4, lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f);
+            named_bar_sync(bar_id, 64);
+            if (lt == 0) mbar_arrive(raw_empty + 8 * rs);
+
+            // A (warp 0) and P (warp 1): [K|Q] * 2^(G - G_mid) times (K * 2^(G_mid - G))^T, tf32
+            {
+                const uint32_t X = scr + (lw == 0 ? S_KL : S_QL);
+                float acc[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {
+                    const int cc = 8 * ks + t;
+                    const float a0 = ldsf(X + g * F_LD + cc * 4), a1 = ldsf(X + (g + 8) * F_LD + cc * 4);
+                    const float a2 = ldsf(X + g * F_LD + (cc + 4) * 4), a3 = ldsf(X + (g + 8) * F_LD + (cc + 4) * 4);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float b0 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + cc * 4);
+                        const float b1 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + (cc + 4) * 4);
+                        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                if (lw == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
+                            const float br = ldsf(scr + S_BETA + r * 4);
+                            stsf(scr + S_AM + r * A_LD + j * 4, j < r ? acc[nt][i] * br : 0.f);
+                        }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh, j = 8 * nt + 2 * t;
+                            const float v0 = j <= r ? acc[nt][2 * hh] : 0.f;
+                            const float v1 = j + 1 <= r ? acc[nt][2 * hh + 1] : 0.f;
+                            sts32(pslot + P_PP + r * SM_LD + j * 2, pack_f16(v0, v1));
+                        }
+                }
+            }
+            named_bar_sync(bar_id, 64);
+
+            // T = (I + A)^-1 by forward substitution; lane c (mod 16) owns column c
+            if (lw == 0) {
+                const int c = lane & 15;
+                float tc[CHUNK];
+#pragma unroll
+                for (int r = 0; r < CHUNK; ++r) {
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int j4 = 0; j4 < r; j4 += 4) {
+                        const float4 a = ldsf4(scr + S_AM + r * A_LD + j4 * 4);
+                        if (j4 + 0 < r) s0 = fmaf(a.x, tc[j4 + 0], s0);
+                        if (j4 + 1 < r) s1 = fmaf(a.y, tc[j4 + 1], s1);
+                        if (j4 + 2 < r) s2 = fmaf(a.z, tc[j4 + 2], s2);
+                        if (j4 + 3 < r) s3 = fmaf(a.w, tc[j4 + 3], s3);
+                    }
+                    tc[r] = (r == c ? 1.f : 0.f) - ((s0 + s1) + (s2 + s3));
+                }
+                const float bc = ldsf(scr + S_BETA + c * 4);
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    if ((j >> 3) == (lane >> 4)) sts16(pslot + P_TT + j * SM_LD + c * 2, f2h_bits(tc[j] * bc));
+            }
+            const bool stop = named_bar_or(bar_id, 64, failed);
+            if (lt == 0) mbar_arrive(prep_full + 8 * ln);
+            if (stop) break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- scan warps
+    const int sw = warp - 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int vr0 = slice * (16 * NS) + 16 * sw;
+    const size_t st_base = (static_cast<size_t>(seq) * p.H + h) * (DH * DH);
+    float S[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
+            float x = 0.f, y = 0.f;
+            if (p.init) {
+                if (p.init_dtype == KDA_DTYPE_FP32) {
+                    const float2 w = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.init) + e);
+                    x = w.x;
+                    y = w.y;
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(p.init) + e);
+                    x = bf16_lo(w);
+                    y = bf16_hi(w);
+                }
+            }
+            S[nt][2 * hh] = x;
+            S[nt][2 * hh + 1] = y;
+        }
+
+    const int mi = lane >> 3, ri = lane & 7;
+    for (int n = 0; n < nch; ++n) {
+        const int ps = n % NP, rs = n % NR;
+        const uint32_t pph = (n / NP) & 1, rph = (n / NR) & 1;
+        bool ok = wait_bar(prep_full + 8 * ps, pph, flags);
+        ok = ok && wait_bar(raw_full + 8 * rs, rph, flags);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int tok0 = sp.bos + n * CHUNK;
+        const int Lv = min(CHUNK, sp.len - n * CHUNK);
+        const uint32_t pb = sb + OFF_PREP + ps * PREP_SLOT;
+        const uint32_t vt = sb + OFF_RAW + rs * RAW_STAGE + OFF_V;
+
+        // Z = S [K*Gamma ; Q*Gamma]^T  (16 rows x 32 columns per warp)
+        float z[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) z[i][0] = z[i][1] = z[i][2] = z[i][3] = 0.f;
+        const uint32_t bz = pb + P_BZ + (ri + 8 * (mi >> 1)) * BZ_LD + 16 * (mi & 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a[4] = {pack_bf16(S[2 * kk][0], S[2 * kk][1]), pack_bf16(S[2 * kk][2], S[2 * kk][3]),
+                                   pack_bf16(S[2 * kk + 1][0], S[2 * kk + 1][1]),
+                                   pack_bf16(S[2 * kk + 1][2], S[2 * kk + 1][3])};
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(bz + kk * 32, b0, b1, b2, b3);
+            mma_bf16(z[0], a, b0, b1);
+            mma_bf16(z[1], a, b2, b3);
+            ldsm_x4(bz + 16 * BZ_LD + kk * 32, b0, b1, b2, b3);
+            mma_bf16(z[2], a, b0, b1);
+            mma_bf16(z[3], a, b2, b3);
+        }
+
+        // R = V^T - Z_k (rows past the chunk's end are zero)
+        float R[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 8 * nt + 2 * t + (i & 1), vr = vr0 + g + 8 * (i >> 1);
+                const float vv = j < Lv ? __uint_as_float(static_cast<uint32_t>(lds16(vt + raw_off(j, vr))) << 16) : 0.f;
+                R[nt][i] = vv - z[nt][i];
+            }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+
+        // E = R (T diag(beta))^T
+        const uint32_t ra[4] = {pack_f16(R[0][0], R[0][1]), pack_f16(R[0][2], R[0][3]), pack_f16(R[1][0], R[1][1]),
+                                pack_f16(R[1][2], R[1][3])};
+        float e[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            e[nt][0] = e[nt][1] = e[nt][2] = e[nt][3] = 0.f;
+            const uint32_t row = pb + P_TT + (8 * nt + g) * SM_LD + 4 * t;
+            mma_f16(e[nt], ra, lds32(row), lds32(row + 16));
+        }
+        const uint32_t ea[4] = {pack_f16(e[0][0], e[0][1]), pack_f16(e[0][2], e[0][3]), pack_f16(e[1][0], e[1][1]),
+                                pack_f16(e[1][2], e[1][3])};
+
+        // O = scale (Z_q + E P^T)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t row = pb + P_PP + (8 * nt + g) * SM_LD + 4 * t;
+            mma_f16(z[2 + nt], ea, lds32(row), lds32(row + 16));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 8 * nt + 2 * t + (i & 1), vr = vr0 + g + 8 * (i >> 1);
+                if (r < Lv) p.out[(static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr] = f2bf_bits(p.scale * z[2 + nt][i]);
+            }
+
+        // S = S Diag(gamma) + E Kbar
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const float2 gm = ldsf2(pb + P_GAM + (8 * nt + 2 * t) * 4);
+            S[nt][0] *= gm.x;
+            S[nt][1] *= gm.y;
+            S[nt][2] *= gm.x;
+            S[nt][3] *= gm.y;
+        }
+        const uint32_t kb = pb + P_KB + (ri + 8 * (mi & 1)) * BZ_LD + 16 * (mi >> 1);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(kb + m * 32, b0, b1, b2, b3);
+            mma_f16(S[2 * m], ea, b0, b1);
+            mma_f16(S[2 * m + 1], ea, b2, b3);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(prep_empty + 8 * ps);
+    }
+
+    if (p.fin) {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
+                if (p.fin_dtype == KDA_DTYPE_FP32)
+                    *reinterpret_cast<float2 *>(static_cast<float *>(p.fin) + e) = make_float2(S[nt][2 * hh], S[nt][2 * hh + 1]);
+                else
+                    *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(p.fin) + e) = pack_bf16(S[nt][2 * hh], S[nt][2 * hh + 1]);
+            }
+    }
+}
+
+
+}  // namespace v1
+}  // namespace kda

@@ -1,0 +1,661 @@
+// kda_fwd_tc.cuh -- KDA forward pass with the state products on the 5th-gen
+// tensor core (tcgen05) and the fp32 state held in tensor memory. One CTA
+// per (sequence, head) state, all 128 V rows.
+//
+// Chunk algebra. For chunk n (16 tokens) with state S_n (V x K) at its start,
+// the prep lanes reduce the chunk to
+//   WX_n = [-w_n ; s q^_n] (32 x K),  TM_n = [T'_n ; s M_n] (32 x 16),
+//   Kbar_n (16 x K), gamma_n (K), V_n,
+// with T' = (I + A)^-1 diag(beta), w = T' (K*Gamma), M = P T',
+// q^ = Q*Gamma - M (K*Gamma), s = scale, so that one product gives both the
+// rows written into the state and the outputs:
+//   [E_n | O_n] = D_n = V_n^T TM_n^T + S_n WX_n^T,
+//   S_{n+1} = S_n Diag(gamma_n) + E_n Kbar_n.
+// The state product S_n WX_n^T streams the whole 128x128 state through the
+// tensor core; to keep it off the per-chunk dependency chain it is formed two
+// chunks ahead, from the decayed state two chunks back, and corrected by the
+// two rank-16 updates in between (exact in real arithmetic):
+//   S_n WX_n^T = bf16(S_{n-2} Gamma_{n-2}) WY_n^T + E_{n-2} C'_{n-2} + E_{n-1} C_{n-1},
+//   WY_n = WX_n Diag(gamma_{n-1}),  C_{n-1} = Kbar_{n-1} WX_n^T,
+//   C'_{n-2} = Kbar_{n-2} WY_n^T.
+// Only the last term depends on the previous chunk's result, so each chunk's
+// critical path is one 16-deep MMA plus one commit.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer (lane 0); allocates / frees tensor memory.
+//   warp 1      MMA issuer (lane 0).
+//   warps 2-5   state warps, one V row per thread (tensor-memory lane):
+//               read [E|O], hand E to the tensor core, decay the state
+//               (S <- S Diag(gamma)) and keep its bf16 copy, store outputs.
+//   warps 6-9   two prep lanes of two warps, alternate chunks.
+// Tensor memory (512 columns): state fp32 [0,128), D x3 [128,224),
+// E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384).
+//
+// Page references: base-2 gate with the LOG2E-folded scale and the tanh form
+// of the sigmoid ("FlashKDA lower_bound Parameter ..." -- "Conversion to the
+// Gate Scale Factor"; "Base-2 Exponent Optimization in FlashKDA ..." --
+// "Re-basing the Gate Activation"), CHUNK = 16 and the unit-lower chunk
+// inverse ("How FlashKDA's CHUNK Size of 16 ..." -- "Efficient 16x16 Matrix
+// Inversion"), tensor contract ("FlashKDA Input Tensor Shapes and DTypes ...").
+#pragma once
+#include "kda_common.cuh"
+#include "tcgen05.cuh"
+
+namespace kda {
+namespace tcs {
+
+constexpr int NR = 4;  // raw chunk ring
+constexpr int NP = 4;  // prep slot ring
+constexpr int NTHREADS = 320;
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_S = 0;     // fp32 state, 128 columns
+constexpr uint32_t T_D = 128;   // D[3], 32 columns each
+constexpr uint32_t T_E = 224;   // E[2], 8 columns each (16 f16)
+constexpr uint32_t T_SB = 256;  // bf16 state copies [2], 64 columns each
+
+// prep slot (bytes)
+constexpr int L_WY = 0;        // bf16, K-major 128B swizzle: 2 K-blocks x [32 rows][128 B]
+constexpr int L_V16 = 8192;    // f16 V, MN-major 128B swizzle: 2 boxes x [16 rows][128 B]
+constexpr int L_KB = 12288;    // f16 Kbar [128 n][16 k], K-major core matrices
+constexpr int L_TM = 16384;    // f16 [32 n][16 k]
+constexpr int L_CC = 17408;    // f16 C_{n-1}^T [32 n][16 k]
+constexpr int L_CP = 18432;    // f16 C'_{n-2}^T [32 n][16 k]
+constexpr int L_GAM = 19456;   // fp32 gamma [128]
+constexpr int SLOT = 20480;
+
+// prep scratch (per lane)
+constexpr int F_LD = 528;  // fp32 [16][132]
+constexpr int A_LD = 80;   // fp32 [16][20]
+constexpr int H_LD = 272;  // f16 [16][136]
+constexpr int M_LD = 48;   // f16 [16][24]
+constexpr int S_KL = 0;
+constexpr int S_QL = 16 * F_LD;
+constexpr int S_KR = 32 * F_LD;
+constexpr int S_AM = 48 * F_LD;
+constexpr int S_BETA = S_AM + 16 * A_LD;
+constexpr int S_KG = S_BETA + 64;
+constexpr int S_QG = S_KG + 16 * H_LD;
+constexpr int S_TP = S_QG + 16 * H_LD;
+constexpr int S_PP = S_TP + 16 * M_LD;
+constexpr int SCR = S_PP + 16 * M_LD;
+
+constexpr int OFF_RAW = 0;
+constexpr int OFF_SLOT = OFF_RAW + NR * RAW_STAGE;
+constexpr int OFF_SCR = OFF_SLOT + NP * SLOT;
+constexpr int OFF_BAR = OFF_SCR + 2 * SCR;
+// barrier indices
+constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_PREP_FULL = 8, B_PREP_EMPTY = 12, B_D = 16, B_E = 18, B_G = 20,
+              B_S = 22, B_I = 24, B_F = 25, NBARS = 26;
+constexpr int OFF_TMEMPTR = OFF_BAR + NBARS * 8;
+constexpr int OFF_FLAGS = OFF_TMEMPTR + 16;
+constexpr int SMEM_USED = OFF_FLAGS + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+
+static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && SCR % 16 == 0, "ldmatrix alignment");
+static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+
+// byte offset of (row n, col k) in a K-major, non-swizzled f16 operand with
+// 16 K elements per row: 8x8 core matrices, LBO = 128 (K), SBO = 256 (N)
+__device__ __forceinline__ uint32_t cm16(int n, int k)
+{
+    return (n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
+}
+// byte offset of (row, col) in a bf16 K-major 128B-swizzled operand, K = 128
+// as two 64-column blocks of 32 rows
+__device__ __forceinline__ uint32_t sw128_32rows(int row, int c)
+{
+    return (c >> 6) * 4096 + row * 128 + ((((c & 63) >> 3) ^ (row & 7)) << 4) + (c & 7) * 2;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
+{
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seq = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const Span sp = seq_span(p, seq);
+    if (threadIdx.x == 0) {
+        if (p.cu && blockIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.nseq] != p.total)) atomicOr(&g_dev_error, DEVERR_SEQLENS);
+        if (!sp.ok && h == 0) atomicOr(&g_dev_error, DEVERR_SEQLENS);
+    }
+    if (!sp.ok) return;  // CTA-uniform, before any tensor memory is taken
+    const int nch = (sp.len + CHUNK - 1) / CHUNK;
+
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
+    auto bar = [&](int i) { return sb + OFF_BAR + 8 * i; };
+    auto slot = [&](int n) { return sb + OFF_SLOT + (n % NP) * SLOT; };
+
+    if (warp == 0) {
+        tc::alloc(sb + OFF_TMEMPTR, TMEM_COLS);
+        tc::relinquish();
+    }
+    if (threadIdx.x == 32) {
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(bar(B_RAW_FULL + i), 1);
+            mbar_init(bar(B_RAW_EMPTY + i), 1);
+        }
+        for (int i = 0; i < NP; ++i) {
+            mbar_init(bar(B_PREP_FULL + i), 1);
+            mbar_init(bar(B_PREP_EMPTY + i), 2);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_D + i), 1);
+            mbar_init(bar(B_E + i), 4);
+            mbar_init(bar(B_G + i), 4);
+            mbar_init(bar(B_S + i), 1);
+        }
+        mbar_init(bar(B_I), 4);
+        mbar_init(bar(B_F), 1);
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEMPTR);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            tma_prefetch_desc(&tg);
+            int n = 0;
+            for (; n < nch; ++n) {
+                const int s = n % NR;
+                if (!wait_bar(bar(B_RAW_EMPTY + s), ((n / NR) & 1) ^ 1, flags)) break;
+                const uint32_t fb = bar(B_RAW_FULL + s);
+                mbar_arrive_expect_tx(fb, RAW_STAGE);
+                const int tok = sp.bos + n * CHUNK;
+                const uint32_t dst = sb + OFF_RAW + s * RAW_STAGE;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(dst + OFF_Q + b * RAW_BOX, &tq, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_K + b * RAW_BOX, &tk, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_V + b * RAW_BOX, &tv, 64 * b, h, tok, fb);
+                    tma_load_3d(dst + OFF_G + b * RAW_BOX, &tg, 64 * b, h, tok, fb);
+                }
+            }
+            for (int m = (n > NR ? n - NR : 0); m < n; ++m) drain_bar(bar(B_RAW_FULL + m % NR), (m / NR) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0 && nch > 0) {
+            const uint32_t id_u = tc::idesc(tc::F16, 128, 32, 1, 0);
+            const uint32_t id_c = tc::idesc(tc::F16, 128, 32, 0, 0);
+            const uint32_t id_y = tc::idesc(tc::BF16, 128, 32, 0, 0);
+            const uint32_t id_s = tc::idesc(tc::F16, 128, 128, 0, 0);
+            // D_n = V_n^T TM_n^T (fresh)
+            auto issue_u = [&](int n) {
+                const uint32_t sl = slot(n);
+                tc::mma_ss(tmem + T_D + 32 * (n % 3), tc::sdesc(sl + L_V16, 2048, 1024, tc::SWZ_128B),
+                           tc::sdesc(sl + L_TM, 128, 256, tc::SWZ_NONE), id_u, 0);
+            };
+            // D_n += Sb[b] WY_n^T
+            auto issue_y = [&](int n, int b) {
+                const uint32_t sl = slot(n);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    tc::mma_ts(tmem + T_D + 32 * (n % 3), tmem + T_SB + 64 * b + 8 * i,
+                               tc::sdesc(sl + L_WY + (i >> 2) * 4096 + (i & 3) * 32, 16, 1024, tc::SWZ_128B), id_y, 1);
+            };
+            bool ok = wait_bar(bar(B_I), 0, flags);
+            for (int n = 0; ok && n < (nch < 2 ? nch : 2); ++n) {
+                ok = wait_bar(bar(B_PREP_FULL + n % NP), (n / NP) & 1, flags);
+                if (!ok) break;
+                tc::fence_after();
+                issue_u(n);
+                issue_y(n, n & 1);
+                if (n == 0) tc::commit(bar(B_D + 0));
+            }
+            for (int k = 0; ok && k < nch; ++k) {
+                ok = wait_bar(bar(B_E + (k & 1)), (k >> 1) & 1, flags);
+                if (!ok) break;
+                tc::fence_after();
+                const uint32_t e = tmem + T_E + 8 * (k & 1);
+                if (k + 1 < nch) {  // D_{k+1} += E_k C_k
+                    tc::mma_ts(tmem + T_D + 32 * ((k + 1) % 3), e, tc::sdesc(slot(k + 1) + L_CC, 128, 256, tc::SWZ_NONE),
+                               id_c, 1);
+                    tc::commit(bar(B_D + ((k + 1) & 1)));
+                }
+                ok = wait_bar(bar(B_G + (k & 1)), (k >> 1) & 1, flags);
+                if (!ok) break;
+                tc::fence_after();
+                // S += E_k Kbar_k (the state was decayed in place by the state warps)
+                tc::mma_ts(tmem + T_S, e, tc::sdesc(slot(k) + L_KB, 128, 256, tc::SWZ_NONE), id_s, 1);
+                tc::commit(bar(B_S + (k & 1)));
+                tc::commit(bar(B_PREP_EMPTY + k % NP));
+                if (k + 2 < nch) {  // D_{k+2} = U + E_k C'_k + Sb[k] WY^T
+                    const int n = k + 2;
+                    ok = wait_bar(bar(B_PREP_FULL + n % NP), (n / NP) & 1, flags);
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_u(n);
+                    tc::mma_ts(tmem + T_D + 32 * (n % 3), e, tc::sdesc(slot(n) + L_CP, 128, 256, tc::SWZ_NONE), id_c, 1);
+                    issue_y(n, k & 1);
+                }
+            }
+            tc::commit(bar(B_F));
+            drain_bar(bar(B_F), 0);
+        }
+    } else if (warp < 6) {
+        // ---------------------------------------------------------------- state warps
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;
+        const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        const size_t st_row = (static_cast<size_t>(seq) * p.H + h) * (DH * DH) + static_cast<size_t>(row) * DH;
+#pragma unroll 1
+        for (int g4 = 0; g4 < 4; ++g4) {
+            uint32_t r32[32], r16[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.init) {
+                    if (p.init_dtype == KDA_DTYPE_FP32) {
+                        v = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + st_row + 32 * g4 + i);
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.init) + st_row + 32 * g4 + i);
+                        v = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                    }
+                }
+                r32[i] = __float_as_uint(v.x);
+                r32[i + 1] = __float_as_uint(v.y);
+                r32[i + 2] = __float_as_uint(v.z);
+                r32[i + 3] = __float_as_uint(v.w);
+                r16[i / 2] = pack_bf16(v.x, v.y);
+                r16[i / 2 + 1] = pack_bf16(v.z, v.w);
+            }
+            tc::st32(lb + T_S + 32 * g4, r32);
+            tc::st16(lb + T_SB + 16 * g4, r16);
+            tc::st16(lb + T_SB + 64 + 16 * g4, r16);
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_I));
+
+        bool ok = true;
+        for (int k = 0; k < nch; ++k) {
+            ok = wait_bar(bar(B_D + (k & 1)), (k >> 1) & 1, flags);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            uint32_t d[32];
+            tc::ld32(lb + T_D + 32 * (k % 3), d);
+            tc::wait_ld();
+            {  // E_k (f16) -> tensor memory, then release the chain
+                uint32_t e8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e8[i] = pack_f16(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+                tc::st8(lb + T_E + 8 * (k & 1), e8);
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_E + (k & 1)));
+            }
+            // decay the state for this chunk: S <- S Diag(gamma_k), and its bf16 copy
+            ok = (k == 0) || wait_bar(bar(B_S + ((k - 1) & 1)), ((k - 1) >> 1) & 1, flags);
+            ok = ok && wait_bar(bar(B_PREP_FULL + k % NP), (k / NP) & 1, flags);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            const uint32_t gam = slot(k) + L_GAM;
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint32_t r32[32], r16[16];
+                tc::ld32(lb + T_S + 32 * g4, r32);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 gv = ldsf4(gam + (32 * g4 + i) * 4);
+                    const float a0 = __uint_as_float(r32[i]) * gv.x, a1 = __uint_as_float(r32[i + 1]) * gv.y;
+                    const float a2 = __uint_as_float(r32[i + 2]) * gv.z, a3 = __uint_as_float(r32[i + 3]) * gv.w;
+                    r32[i] = __float_as_uint(a0);
+                    r32[i + 1] = __float_as_uint(a1);
+                    r32[i + 2] = __float_as_uint(a2);
+                    r32[i + 3] = __float_as_uint(a3);
+                    r16[i / 2] = pack_bf16(a0, a1);
+                    r16[i / 2 + 1] = pack_bf16(a2, a3);
+                }
+                tc::st32(lb + T_S + 32 * g4, r32);
+                tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);
+            }
+            tc::wait_st();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_G + (k & 1)));
+            // outputs (already scaled)
+            const int tok0 = sp.bos + k * CHUNK;
+            const int Lv = min(CHUNK, sp.len - k * CHUNK);
+#pragma unroll
+            for (int r = 0; r < CHUNK; ++r)
+                if (r < Lv)
+                    p.out[(static_cast<size_t>(tok0 + r) * p.H + h) * DH + row] = f2bf_bits(__uint_as_float(d[16 + r]));
+        }
+        if (p.fin) {
+            if (ok && nch > 0) ok = wait_bar(bar(B_S + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1, flags);
+            ok = __all_sync(0xffffffffu, ok);
+            tc::fence_after();
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint32_t r32[32];
+                tc::ld32(lb + T_S + 32 * g4, r32);
+                tc::wait_ld();
+                if (p.fin_dtype == KDA_DTYPE_FP32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + st_row + 32 * g4);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r32[4 * i]), __uint_as_float(r32[4 * i + 1]),
+                                             __uint_as_float(r32[4 * i + 2]), __uint_as_float(r32[4 * i + 3]));
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.fin) + st_row + 32 * g4);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack_bf16(__uint_as_float(r32[8 * i]), __uint_as_float(r32[8 * i + 1])),
+                                            pack_bf16(__uint_as_float(r32[8 * i + 2]), __uint_as_float(r32[8 * i + 3])),
+                                            pack_bf16(__uint_as_float(r32[8 * i + 4]), __uint_as_float(r32[8 * i + 5])),
+                                            pack_bf16(__uint_as_float(r32[8 * i + 6]), __uint_as_float(r32[8 * i + 7])));
+                }
+            }
+        }
+        tc::fence_before();
+    } else {
+        // ---------------------------------------------------------------- prep lanes
+        const int ln = (warp - 6) >> 1;
+        const int lt = threadIdx.x - 192 - 64 * ln;  // 0..63
+        const int lw = lt >> 5;
+        const uint32_t bar_id = 1 + ln;
+        const uint32_t scr = sb + OFF_SCR + ln * SCR;
+        const int c0 = 2 * lt;
+        float a_h = 1.f, bias0 = 0.f, bias1 = 0.f;
+        if (p.A_log) a_h = ex2_approx(__ldg(p.A_log + h) * LOG2E);
+        if (p.dt_bias) {
+            bias0 = __ldg(p.dt_bias + h * DH + c0);
+            bias1 = __ldg(p.dt_bias + h * DH + c0 + 1);
+        }
+        const float hs = p.half_gs, sc = p.scale;
+        const int g = lane >> 2, t = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+
+        for (int n = ln; n < nch; n += 2) {
+            bool failed = false;
+            const int rs = n % NR;
+            const uint32_t sl = slot(n);
+            const int tok0 = sp.bos + n * CHUNK;
+            const int Lv = min(CHUNK, sp.len - n * CHUNK);
+            float blogit = 0.f;
+            if (lw == 1 && lane < Lv)
+                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lane) * p.H + h)) << 16);
+            if (!wait_bar(bar(B_RAW_FULL + rs), (n / NR) & 1, flags)) failed = true;
+            const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
+
+            // gate (log2 units) and its inclusive in-chunk cumsum
+            float G0[CHUNK], G1[CHUNK];
+            {
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int r = 0; r < CHUNK; ++r) {
+                    const uint32_t gw = lds32(raw + OFF_G + raw_off(r, c0));
+                    const float x0 = a_h * (bf16_lo(gw) + bias0), x1 = a_h * (bf16_hi(gw) + bias1);
+                    const float ga0 = fmaf(hs, tanh_approx(0.5f * x0), hs);
+                    const float ga1 = fmaf(hs, tanh_approx(0.5f * x1), hs);
+                    acc0 += (r < Lv) ? ga0 : 0.f;
+                    acc1 += (r < Lv) ? ga1 : 0.f;
+                    G0[r] = acc0;
+                    G1[r] = acc1;
+                }
+            }
+            if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
+
+            const float Gm0 = G0[7], Gm1 = G1[7];
+            const float sm0 = ex2_approx(-Gm0) * TRUNC_COMP, sm1 = ex2_approx(-Gm1) * TRUNC_COMP;
+            const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
+            stsf2(sl + L_GAM + c0 * 4, ex2_approx(G0[15]), ex2_approx(G1[15]));
+            float kb0[CHUNK], kb1[CHUNK];
+#pragma unroll
+            for (int r = 0; r < CHUNK; ++r) {
+                const uint32_t kw = lds32(raw + OFF_K + raw_off(r, c0));
+                const uint32_t qw = lds32(raw + OFF_Q + raw_off(r, c0));
+                const uint32_t vw = lds32(raw + OFF_V + raw_off(r, c0));
+                const bool live = r < Lv;
+                const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
+                const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
+                const float v0 = live ? bf16_lo(vw) : 0.f, v1 = live ? bf16_hi(vw) : 0.f;
+                const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);
+                const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);
+                const float kg0 = k0 * gm0, kg1 = k1 * gm1, qg0 = q0 * gm0, qg1 = q1 * gm1;
+                sts32(scr + S_KG + r * H_LD + c0 * 2, pack_f16(kg0, kg1));
+                sts32(scr + S_QG + r * H_LD + c0 * 2, pack_f16(qg0, qg1));
+                sts32(sl + L_V16 + raw_off(r, c0), pack_f16(v0, v1));
+                stsf2(scr + S_KL + r * F_LD + c0 * 4, kg0 * sm0, kg1 * sm1);
+                stsf2(scr + S_QL + r * F_LD + c0 * 4, qg0 * sm0, qg1 * sm1);
+                const float kr0 = k0 * f0, kr1 = k1 * f1;
+                stsf2(scr + S_KR + r * F_LD + c0 * 4, kr0 * TRUNC_COMP, kr1 * TRUNC_COMP);
+                kb0[r] = kr0 * se0;
+                kb1[r] = kr1 * se1;
+            }
+            {  // Kbar as the K-major [c][j] operand: two 16-byte rows per channel
+                uint32_t w0[8], w1[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w0[i] = pack_f16(kb0[2 * i], kb0[2 * i + 1]);
+                    w1[i] = pack_f16(kb1[2 * i], kb1[2 * i + 1]);
+                }
+                const uint32_t a0 = sl + L_KB + cm16(c0, 0), a1 = sl + L_KB + cm16(c0 + 1, 0);
+                sts128(a0, w0[0], w0[1], w0[2], w0[3]);
+                sts128(a0 + 128, w0[4], w0[5], w0[6], w0[7]);
+                sts128(a1, w1[0], w1[1], w1[2], w1[3]);
+                sts128(a1 + 128, w1[4], w1[5], w1[6], w1[7]);
+            }
+            if (lw == 1 && lane < CHUNK)
+                stsf(scr + S_BETA + lane * 4, lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f);
+            named_bar_sync(bar_id, 64);
+            if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
+
+            // A (warp 0) and P (warp 1), tf32
+            {
+                const uint32_t X = scr + (lw == 0 ? S_KL : S_QL);
+                float acc[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks) {
+                    const int cc = 8 * ks + t;
+                    const float a0 = ldsf(X + g * F_LD + cc * 4), a1 = ldsf(X + (g + 8) * F_LD + cc * 4);
+                    const float a2 = ldsf(X + g * F_LD + (cc + 4) * 4), a3 = ldsf(X + (g + 8) * F_LD + (cc + 4) * 4);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float b0 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + cc * 4);
+                        const float b1 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + (cc + 4) * 4);
+                        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+                if (lw == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
+                            const float br = ldsf(scr + S_BETA + r * 4);
+                            stsf(scr + S_AM + r * A_LD + j * 4, j < r ? acc[nt][i] * br : 0.f);
+                        }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh, j = 8 * nt + 2 * t;
+                            const float v0 = j <= r ? acc[nt][2 * hh] : 0.f;
+                            const float v1 = j + 1 <= r ? acc[nt][2 * hh + 1] : 0.f;
+                            sts32(scr + S_PP + r * M_LD + j * 2, pack_f16(v0, v1));
+                        }
+                }
+            }
+            named_bar_sync(bar_id, 64);
+
+            // T' = (I + A)^-1 diag(beta) by forward substitution (warp 0); lane c (mod 16) owns column c
+            if (lw == 0) {
+                const int c = lane & 15;
+                float tc_[CHUNK];
+#pragma unroll
+                for (int r = 0; r < CHUNK; ++r) {
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int j4 = 0; j4 < r; j4 += 4) {
+                        const float4 a = ldsf4(scr + S_AM + r * A_LD + j4 * 4);
+                        if (j4 + 0 < r) s0 = fmaf(a.x, tc_[j4 + 0], s0);
+                        if (j4 + 1 < r) s1 = fmaf(a.y, tc_[j4 + 1], s1);
+                        if (j4 + 2 < r) s2 = fmaf(a.z, tc_[j4 + 2], s2);
+                        if (j4 + 3 < r) s3 = fmaf(a.w, tc_[j4 + 3], s3);
+                    }
+                    tc_[r] = (r == c ? 1.f : 0.f) - ((s0 + s1) + (s2 + s3));
+                }
+                const float bc = ldsf(scr + S_BETA + c * 4);
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    if ((j >> 3) == (lane >> 4)) {
+                        const uint16_t hv = f2h_bits(tc_[j] * bc);
+                        sts16(scr + S_TP + j * M_LD + c * 2, hv);
+                        sts16(sl + L_TM + cm16(j, c), hv);
+                    }
+            }
+            named_bar_sync(bar_id, 64);
+
+            // WX rows: warp 0 -> -w = -T' (K*Gamma); warp 1 -> s q^ = s (Q*Gamma) - s M (K*Gamma)
+            float acc[16][4];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            {
+                uint32_t aX[4];
+                if (lw == 0) {
+                    ldsm_x4(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aX[0], aX[1], aX[2], aX[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) aX[i] ^= 0x80008000u;
+                } else {
+                    // M = P T' (16 x 16 x 16); also TM rows 16..31 = s M
+                    uint32_t aP[4], b0, b1, b2, b3;
+                    ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
+                    ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
+                    float m[2][4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) m[i][0] = m[i][1] = m[i][2] = m[i][3] = 0.f;
+                    mma_f16(m[0], aP, b0, b1);
+                    mma_f16(m[1], aP, b2, b3);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh, col = 8 * nt + 2 * t;
+                            sts32(sl + L_TM + cm16(16 + r, col), pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]));
+                        }
+                    aX[0] = pack_f16(-sc * m[0][0], -sc * m[0][1]);
+                    aX[1] = pack_f16(-sc * m[0][2], -sc * m[0][3]);
+                    aX[2] = pack_f16(-sc * m[1][0], -sc * m[1][1]);
+                    aX[3] = pack_f16(-sc * m[1][2], -sc * m[1][3]);
+                }
+#pragma unroll
+                for (int m8 = 0; m8 < 8; ++m8) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(scr + S_KG + (ri + 8 * (mi & 1)) * H_LD + 32 * m8 + 16 * (mi >> 1), b0, b1, b2, b3);
+                    mma_f16(acc[2 * m8], aX, b0, b1);
+                    mma_f16(acc[2 * m8 + 1], aX, b2, b3);
+                }
+                if (lw == 1) {
+                    // + s * I * (Q*Gamma)
+                    const uint32_t sh = static_cast<uint32_t>(f2h_bits(sc));
+                    uint32_t aI[4];
+                    aI[0] = (g == 2 * t ? sh : 0u) | (g == 2 * t + 1 ? sh << 16 : 0u);
+                    aI[1] = 0u;
+                    aI[2] = 0u;
+                    aI[3] = aI[0];
+#pragma unroll
+                    for (int m8 = 0; m8 < 8; ++m8) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(scr + S_QG + (ri + 8 * (mi & 1)) * H_LD + 32 * m8 + 16 * (mi >> 1), b0, b1, b2, b3);
+                        mma_f16(acc[2 * m8], aI, b0, b1);
+                        mma_f16(acc[2 * m8 + 1], aI, b2, b3);
+                    }
+                }
+            }
+
+            // cross-chunk terms: gamma_{n-1}, Kbar_{n-1}, Kbar_{n-2}
+            if (n >= 1 && !wait_bar(bar(B_PREP_FULL + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+            const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
+            const int rowA = 16 * lw + g;
+            float cacc[2][4], pacc[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                cacc[i][0] = cacc[i][1] = cacc[i][2] = cacc[i][3] = 0.f;
+                pacc[i][0] = pacc[i][1] = pacc[i][2] = pacc[i][3] = 0.f;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                // WX / WY columns c in [16 kk, 16 kk + 16)
+                uint32_t bx[2][2], by[2][2];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int nt = 2 * kk + half, c = 8 * nt + 2 * t;
+                    const float2 gv = n >= 1 ? ldsf2(prev + L_GAM + c * 4) : make_float2(1.f, 1.f);
+                    const float y0 = acc[nt][0] * gv.x, y1 = acc[nt][1] * gv.y;
+                    const float y2 = acc[nt][2] * gv.x, y3 = acc[nt][3] * gv.y;
+                    sts32(sl + L_WY + sw128_32rows(rowA, c), pack_bf16(y0, y1));
+                    sts32(sl + L_WY + sw128_32rows(rowA + 8, c), pack_bf16(y2, y3));
+                    bx[0][half] = pack_f16(acc[nt][0], acc[nt][1]);
+                    bx[1][half] = pack_f16(acc[nt][2], acc[nt][3]);
+                    by[0][half] = pack_f16(y0, y1);
+                    by[1][half] = pack_f16(y2, y3);
+                }
+                const uint32_t koff = (2 * kk + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                if (n >= 1) {
+                    uint32_t aK[4];
+                    ldsm_x4_t(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                    mma_f16(cacc[0], aK, bx[0][0], bx[0][1]);
+                    mma_f16(cacc[1], aK, bx[1][0], bx[1][1]);
+                }
+                if (n >= 2) {
+                    uint32_t aK[4];
+                    ldsm_x4_t(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                    mma_f16(pacc[0], aK, by[0][0], by[0][1]);
+                    mma_f16(pacc[1], aK, by[1][0], by[1][1]);
+                }
+            }
+            // C^T / C'^T as [n = output column][k = j]
+#pragma unroll
+            for (int nu = 0; nu < 2; ++nu)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = g + 8 * (i >> 1), col = 16 * lw + 8 * nu + 2 * t + (i & 1);
+                    if (n >= 1) sts16(sl + L_CC + cm16(col, j), f2h_bits(cacc[nu][i]));
+                    if (n >= 2) sts16(sl + L_CP + cm16(col, j), f2h_bits(pacc[nu][i]));
+                }
+            tc::fence_async_smem();
+            const bool stop = named_bar_or(bar_id, 64, failed);
+            if (lt == 0) {
+                mbar_arrive(bar(B_PREP_FULL + n % NP));
+                if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));
+            }
+            if (stop) break;
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after();
+        tc::dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace tcs
+}  // namespace kda

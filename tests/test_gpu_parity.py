@@ -49,50 +49,69 @@ def test_split_call_equals_one_call():
     assert_close("final_state", fin.cpu().double().numpy(), s_ref)
 
 
-@pytest.mark.parametrize("T", [1, 15, 17, 37, 100])
-def test_ragged_lengths(T):
-    _check(W.make("b2_t128_h8", T=T, H=3))
+# H = 3 / 4 runs the split-V-row warp-MMA kernel; H = 80 fills the machine
+# with whole-state CTAs and runs the tensor-memory (tcgen05) kernel.
+KERNEL_HEADS = [pytest.param(3, id="mma"), pytest.param(80, id="tcgen05")]
 
 
+def test_head_counts_select_both_kernels():
+    import gated_linear_attention_kda_gb300 as kda
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert kda.plan(3, nsm)[0] > 1 and kda.plan(80, nsm)[0] == 1
+
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 37, 100])
+def test_ragged_lengths(T, H):
+    _check(W.make("b2_t128_h8", T=T, H=H, B=1), heads=None if H < 8 else [0, 41, 79])
+
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
 @pytest.mark.parametrize("lb", [0.0, -0.5, -5.0])
-def test_lower_bound_range(lb):
-    _check(W.make("b2_t128_h8", B=1, H=4), lower_bound=lb)
+def test_lower_bound_range(lb, H):
+    _check(W.make("b2_t128_h8", B=1, H=H, T=70), lower_bound=lb, heads=None if H < 8 else [1, 50])
 
 
-def test_no_gate_parameters_bf16_states():
-    d = W.make("b8_t4096_h16", B=2, T=200, H=5)
-    d["initial_state"] = (torch.randn(2, 5, 128, 128, generator=torch.Generator().manual_seed(9)) * 0.02).to(torch.bfloat16)
-    _check(d, final_dtype="bf16")
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_no_gate_parameters_bf16_states(H):
+    d = W.make("b8_t4096_h16", B=1, T=200, H=H)
+    d["initial_state"] = (torch.randn(1, H, 128, 128, generator=torch.Generator().manual_seed(9)) * 0.02).to(torch.bfloat16)
+    _check(d, final_dtype="bf16", heads=None if H < 8 else [2, 77])
 
 
-def test_in_place_state_equals_out_of_place():
-    d = W.make("b2_t128_h8", T=77)
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_in_place_state_equals_out_of_place(H):
+    d = W.make("b2_t128_h8", T=77, H=H, B=1)
     o1, s1 = run_gpu(d)
     o2, s2 = run_gpu(d, in_place=True)
     assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
 
 
-def test_deterministic_repeats():
-    d = W.make("b2_t128_h8", T=99, H=4)
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_deterministic_repeats(H):
+    d = W.make("b2_t128_h8", T=99, H=H, B=1)
     a = run_gpu(d)
     b = run_gpu(d)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_no_final_state_and_zero_scale():
-    d = W.make("b1_t64_h1")
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_no_final_state_and_zero_scale(H):
+    d = W.make("b1_t64_h1", H=H)
     o, s = run_gpu(d, final_dtype=None, scale=0.0)
     assert s is None and np.all(o == 0)
 
 
-def test_varlen_small_with_empty_and_ragged_sequences():
-    d = W.make("varlen_n16_h32", lengths=[5, 37, 16, 1, 0, 23, 64, 40], H=3)
-    _check(d, final_dtype="bf16")
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_varlen_small_with_empty_and_ragged_sequences(H):
+    d = W.make("varlen_n16_h32", lengths=[5, 37, 16, 1, 0, 23, 64, 40], H=H)
+    _check(d, final_dtype="bf16", heads=None if H < 8 else [0, 33, 79])
 
 
-def test_varlen_equals_separate_calls():
+@pytest.mark.parametrize("H", [2, 80])
+def test_varlen_equals_separate_calls(H):
     lens = [19, 48, 3, 33]
-    d = W.make("varlen_n16_h32", lengths=lens, H=2)
+    d = W.make("varlen_n16_h32", lengths=lens, H=H)
     o, s = run_gpu(d, final_dtype="bf16")
     cu = d["cu_seqlens"]
     for i in range(len(lens)):
