@@ -1,0 +1,142 @@
+// kda_chunk.cuh -- warp-level pieces of the intra-chunk algebra shared by the
+// KDA kernels: the decay-scaled chunk products A = Kl Kr^T and P = Ql Kr^T
+// from bf16 hi/lo operand pairs, and the unit-lower inverse (I + A)^-1 from
+// the nilpotent product form (I - A)(I + A^2)(I + A^4)(I + A^8), all on
+// m16n8k16 warp MMA with register-resident fragments.
+//
+// "How FlashKDA's CHUNK Size of 16 Improves Numerical Stability Over CHUNK
+// 64" -- "Efficient 16x16 Matrix Inversion": 16-token chunks, the unit-lower
+// chunk matrix is inverted by a Neumann series (exact here: A^16 = 0).
+#pragma once
+#include "kda_common.cuh"
+
+namespace kda {
+
+// 8x8 16-bit matrix transpose within a warp (standard fragment layout).
+__device__ __forceinline__ uint32_t movm_t(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// Accumulator fragments of a 16x16 fp32 matrix as two m16n8 tiles: c[nt][i] holds
+// (row g + 8 (i >> 1), col 8 nt + 2 t + (i & 1)), g = lane / 4, t = lane % 4.
+struct Frag16 {
+    float c[2][4];
+};
+
+__device__ __forceinline__ void frag_zero(Frag16 &f)
+{
+#pragma unroll
+    for (int i = 0; i < 2; ++i) f.c[i][0] = f.c[i][1] = f.c[i][2] = f.c[i][3] = 0.f;
+}
+
+// A-operand (m16 x k16, f16) of an accumulator matrix.
+__device__ __forceinline__ void frag_as_a(const Frag16 &f, uint32_t (&a)[4])
+{
+    a[0] = pack_f16(f.c[0][0], f.c[0][1]);
+    a[1] = pack_f16(f.c[0][2], f.c[0][3]);
+    a[2] = pack_f16(f.c[1][0], f.c[1][1]);
+    a[3] = pack_f16(f.c[1][2], f.c[1][3]);
+}
+
+// B-operand (k16 x n8 tiles, f16) of an accumulator matrix X, i.e. B[k][n] = X[k][n]:
+// b[nt][kb] is the transpose of the 8x8 block (rows 8 kb.., cols 8 nt..).
+__device__ __forceinline__ void frag_as_b(const Frag16 &f, uint32_t (&b)[2][2])
+{
+    b[0][0] = movm_t(pack_f16(f.c[0][0], f.c[0][1]));
+    b[0][1] = movm_t(pack_f16(f.c[0][2], f.c[0][3]));
+    b[1][0] = movm_t(pack_f16(f.c[1][0], f.c[1][1]));
+    b[1][1] = movm_t(pack_f16(f.c[1][2], f.c[1][3]));
+}
+
+// x + s I (in place), for accumulator fragments
+__device__ __forceinline__ void frag_add_diag(Frag16 &f, float s, int g, int t)
+{
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (nt == (i >> 1) && g == 2 * t + (i & 1)) f.c[nt][i] += s;
+}
+
+// c = a * b for 16x16x16 (fp32 accumulate into zeroed c)
+__device__ __forceinline__ void frag_mul(Frag16 &c, const uint32_t (&a)[4], const uint32_t (&b)[2][2])
+{
+    frag_zero(c);
+    mma_f16(c.c[0], a, b[0][0], b[0][1]);
+    mma_f16(c.c[1], a, b[1][0], b[1][1]);
+}
+
+// T = (I + A)^-1 for strictly lower A (fp32 fragments in, fp32 fragments out),
+// as (I - A)(I + A^2)(I + A^4)(I + A^8) with f16 operands.
+__device__ __forceinline__ void unit_lower_inverse(const Frag16 &A, Frag16 &T, int g, int t)
+{
+    uint32_t a[4], b[2][2];
+    Frag16 p2, p4, p8, m;
+    frag_as_a(A, a);
+    frag_as_b(A, b);
+    frag_mul(p2, a, b);            // A^2
+    frag_as_a(p2, a);
+    frag_as_b(p2, b);
+    frag_mul(p4, a, b);            // A^4
+    frag_as_a(p4, a);
+    frag_as_b(p4, b);
+    frag_mul(p8, a, b);            // A^8
+    Frag16 x = A;                  // I - A
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x.c[nt][i] = -x.c[nt][i];
+    frag_add_diag(x, 1.f, g, t);
+    frag_add_diag(p2, 1.f, g, t);
+    frag_add_diag(p4, 1.f, g, t);
+    frag_add_diag(p8, 1.f, g, t);
+    frag_as_a(x, a);
+    frag_as_b(p2, b);
+    frag_mul(m, a, b);             // (I - A)(I + A^2)
+    frag_as_a(m, a);
+    frag_as_b(p4, b);
+    frag_mul(x, a, b);             // ... (I + A^4)
+    frag_as_a(x, a);
+    frag_as_b(p8, b);
+    frag_mul(T, a, b);             // ... (I + A^8)
+}
+
+// Split two floats into bf16 hi and lo parts (x ~= hi + lo to ~16 mantissa bits).
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
+}
+
+// acc[nt] (16 rows r x 16 cols j) = sum_c X[r][c] R[j][c] from bf16 hi/lo tiles
+// stored row-major [16][136] (272-byte rows): three bf16 products
+// Xh Rh + Xh Rl + Xl Rh give ~16-bit operand precision with a bf16 exponent range.
+__device__ __forceinline__ void chunk_gram_x3(uint32_t xh, uint32_t xl, uint32_t rh, uint32_t rl, Frag16 &acc,
+                                              int lane)
+{
+    const int mi = lane >> 3, ri = lane & 7;
+    // A operand: rows r = ri + 8 (mi & 1), cols 16 kk + 8 (mi >> 1)
+    const uint32_t aoff = (ri + 8 * (mi & 1)) * 272 + 16 * (mi >> 1);
+    // B operand (rows j, K = c contiguous): n-tile = mi >> 1, k half = mi & 1
+    const uint32_t boff = (ri + 8 * (mi >> 1)) * 272 + 16 * (mi & 1);
+    frag_zero(acc);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t ah[4], al[4], bh[4], bl[4];
+        ldsm_x4(xh + aoff + 32 * kk, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(xl + aoff + 32 * kk, al[0], al[1], al[2], al[3]);
+        ldsm_x4(rh + boff + 32 * kk, bh[0], bh[1], bh[2], bh[3]);
+        ldsm_x4(rl + boff + 32 * kk, bl[0], bl[1], bl[2], bl[3]);
+        mma_bf16(acc.c[0], ah, bh[0], bh[1]);
+        mma_bf16(acc.c[1], ah, bh[2], bh[3]);
+        mma_bf16(acc.c[0], ah, bl[0], bl[1]);
+        mma_bf16(acc.c[1], ah, bl[2], bl[3]);
+        mma_bf16(acc.c[0], al, bh[0], bh[1]);
+        mma_bf16(acc.c[1], al, bh[2], bh[3]);
+    }
+}
+
+}  // namespace kda

@@ -19,11 +19,6 @@ constexpr int RAW_STAGE = 4 * RAW_TILE;
 constexpr int OFF_Q = 0, OFF_K = RAW_TILE, OFF_V = 2 * RAW_TILE, OFF_G = 3 * RAW_TILE;
 
 constexpr float LOG2E = 1.4426950408889634f;
-// tf32 operands are taken from fp32 bit patterns (low mantissa bits ignored).
-// Scaling by 1 + 2^-11 first centres that truncation error on zero.
-constexpr float TRUNC_COMP = 1.00048828125f;
-
-constexpr int SPIN_LIMIT = 1 << 22;
 
 enum : unsigned { DEVERR_SEQLENS = 1u, DEVERR_TIMEOUT = 2u };
 __device__ unsigned int g_dev_error;
@@ -46,14 +41,20 @@ struct Params {
     float half_gs;  // 0.5 * lower_bound * log2(e)
 };
 
-// Bounded wait on an mbarrier phase. Gives up when another role has already
-// given up (abort flag) or after SPIN_LIMIT polls, which flags the device
-// error word; the caller then leaves its loop so the CTA always terminates.
+// Bounded wait on an mbarrier phase. Each poll may suspend the thread for up
+// to WAIT_HINT_NS (it wakes when the phase completes), so a waiting warp costs
+// no issue slots. Gives up when another role has already given up (abort
+// flag) or after WAIT_LIMIT polls (a few seconds at most), which flags the
+// device error word; the caller then leaves its loop so the CTA terminates.
+constexpr uint32_t WAIT_HINT_NS = 20000;
+constexpr int WAIT_LIMIT = 1 << 18;
+
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
 {
+    if (mbar_try_wait(bar, parity)) return true;
 #pragma unroll 1
-    for (int i = 0; i < SPIN_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
         if (*abort_flag) return false;
     }
     atomicOr(&g_dev_error, DEVERR_TIMEOUT);
@@ -65,8 +66,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 {
 #pragma unroll 1
-    for (int i = 0; i < SPIN_LIMIT; ++i)
-        if (mbar_try_wait(bar, parity)) return;
+    for (int i = 0; i < WAIT_LIMIT; ++i)
+        if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return;
     atomicOr(&g_dev_error, DEVERR_TIMEOUT);
 }
 

@@ -2,6 +2,7 @@
 // products (state rows in registers). Used when a state's V rows are split
 // across several CTAs (few states); see kda_fwd_tc.cuh for the tcgen05 kernel.
 #pragma once
+#include "kda_chunk.cuh"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -20,13 +21,14 @@ constexpr int P_PP = P_TT + 16 * SM_LD;           // f16  [16][24]:  P
 constexpr int P_GAM = P_PP + 16 * SM_LD;          // f32  [128]:     gamma = Gamma at chunk end
 constexpr int PREP_SLOT = P_GAM + DH * 4;
 
-constexpr int F_LD = 528;             // row pitch of fp32 [16][132] tiles
-constexpr int A_LD = 80;              // row pitch of fp32 [16][20] tiles
-constexpr int S_KL = 0;               // tf32 K * 2^(G - G_mid)
-constexpr int S_QL = 16 * F_LD;       // tf32 Q * 2^(G - G_mid)
-constexpr int S_KR = 32 * F_LD;       // tf32 K * 2^(G_mid - G)
-constexpr int S_AM = 48 * F_LD;       // fp32 A
-constexpr int S_BETA = S_AM + 16 * A_LD;
+constexpr int H_LD = 272;             // row pitch of 16-bit [16][136] tiles
+constexpr int S_KLH = 0;              // bf16 hi/lo of K * 2^(G - G_mid), Q * 2^(G - G_mid), K * 2^(G_mid - G)
+constexpr int S_KLL = S_KLH + 16 * H_LD;
+constexpr int S_QLH = S_KLL + 16 * H_LD;
+constexpr int S_QLL = S_QLH + 16 * H_LD;
+constexpr int S_KRH = S_QLL + 16 * H_LD;
+constexpr int S_KRL = S_KRH + 16 * H_LD;
+constexpr int S_BETA = S_KRL + 16 * H_LD;
 constexpr int SCR = S_BETA + 64;
 
 constexpr int OFF_RAW = 0;
@@ -48,8 +50,11 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
 {
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    // align to 1024 B by pointer arithmetic on the shared array, so that accesses
+    // through `smem` stay in the shared address space
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
+#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x / p.vsplit, slice = blockIdx.x % p.vsplit;
     const int seq = unit / p.H, h = unit % p.H;
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
                 float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
                 for (int r = 0; r < CHUNK; ++r) {
-                    const uint32_t gw = lds32(raw + OFF_G + raw_off(r, c0));
+                    const uint32_t gw = SM_AT(const uint32_t, raw + OFF_G + raw_off(r, c0));
                     const float x0 = a_h * (bf16_lo(gw) + bias0), x1 = a_h * (bf16_hi(gw) + bias1);
                     // gate_scale * sigmoid(x) = hs + hs * tanh(x / 2)
                     const float ga0 = fmaf(hs, tanh_approx(0.5f * x0), hs);
@@ -158,93 +163,78 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
             if (!wait_bar(prep_empty + 8 * ln, pph ^ 1, flags)) failed = true;
 
             const float Gm0 = G0[7], Gm1 = G1[7];  // mid-chunk reference halves the exponent range
-            const float sm0 = ex2_approx(-Gm0) * TRUNC_COMP, sm1 = ex2_approx(-Gm1) * TRUNC_COMP;
+            const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
             const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
-            stsf2(pslot + P_GAM + c0 * 4, ex2_approx(G0[15]), ex2_approx(G1[15]));
+            SM_AT(float2, pslot + P_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
-                const uint32_t kw = lds32(raw + OFF_K + raw_off(r, c0));
-                const uint32_t qw = lds32(raw + OFF_Q + raw_off(r, c0));
+                const uint32_t kw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
+                const uint32_t qw = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
                 const bool live = r < Lv;
                 const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
                 const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
                 const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);            // Gamma_r
                 const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);  // 2^(G_mid - G_r)
-                sts32(pslot + P_BZ + r * BZ_LD + c0 * 2, pack_bf16(k0 * gm0, k1 * gm1));
-                sts32(pslot + P_BZ + (16 + r) * BZ_LD + c0 * 2, pack_bf16(q0 * gm0, q1 * gm1));
-                sts32(pslot + P_KB + r * BZ_LD + c0 * 2, pack_f16(k0 * f0 * se0, k1 * f1 * se1));
+                SM_AT(uint32_t, pslot + P_BZ + r * BZ_LD + c0 * 2) = pack_bf16(k0 * gm0, k1 * gm1);
+                SM_AT(uint32_t, pslot + P_BZ + (16 + r) * BZ_LD + c0 * 2) = pack_bf16(q0 * gm0, q1 * gm1);
+                SM_AT(uint32_t, pslot + P_KB + r * BZ_LD + c0 * 2) = pack_f16(k0 * f0 * se0, k1 * f1 * se1);
                 const float u0 = gm0 * sm0, u1 = gm1 * sm1;                              // 2^(G_r - G_mid)
-                stsf2(scr + S_KL + r * F_LD + c0 * 4, k0 * u0, k1 * u1);
-                stsf2(scr + S_QL + r * F_LD + c0 * 4, q0 * u0, q1 * u1);
-                stsf2(scr + S_KR + r * F_LD + c0 * 4, k0 * f0 * TRUNC_COMP, k1 * f1 * TRUNC_COMP);
+                const uint32_t o = r * H_LD + c0 * 2;
+                uint32_t hi, lo;
+                split_bf16(k0 * u0, k1 * u1, hi, lo);
+                SM_AT(uint32_t, scr + S_KLH + o) = hi;
+                SM_AT(uint32_t, scr + S_KLL + o) = lo;
+                split_bf16(q0 * u0, q1 * u1, hi, lo);
+                SM_AT(uint32_t, scr + S_QLH + o) = hi;
+                SM_AT(uint32_t, scr + S_QLL + o) = lo;
+                split_bf16(k0 * f0, k1 * f1, hi, lo);
+                SM_AT(uint32_t, scr + S_KRH + o) = hi;
+                SM_AT(uint32_t, scr + S_KRL + o) = lo;
             }
             if (lw == 1 && lane < CHUNK)
-                stsf(scr + S_BETA + lane * 4, lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f);
+                SM_AT(float, scr + S_BETA + lane * 4) = lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
             named_bar_sync(bar_id, 64);
             if (lt == 0) mbar_arrive(raw_empty + 8 * rs);
 
-            // A (warp 0) and P (warp 1): [K|Q] * 2^(G - G_mid) times (K * 2^(G_mid - G))^T, tf32
+            // warp 0: A = strictly-lower(beta_r Kl Kr^T), T' = (I + A)^-1 diag(beta);
+            // warp 1: P = lower(Ql Kr^T). Three bf16 products per entry (hi/lo split).
             {
-                const uint32_t X = scr + (lw == 0 ? S_KL : S_QL);
-                float acc[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const int cc = 8 * ks + t;
-                    const float a0 = ldsf(X + g * F_LD + cc * 4), a1 = ldsf(X + (g + 8) * F_LD + cc * 4);
-                    const float a2 = ldsf(X + g * F_LD + (cc + 4) * 4), a3 = ldsf(X + (g + 8) * F_LD + (cc + 4) * 4);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const float b0 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + cc * 4);
-                        const float b1 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + (cc + 4) * 4);
-                        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
-                    }
-                }
+                Frag16 acc;
+                if (lw == 0)
+                    chunk_gram_x3(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane);
+                else
+                    chunk_gram_x3(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane);
                 if (lw == 0) {
+                    const float bg = SM_AT(const float, scr + S_BETA + g * 4), bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
-                            const float br = ldsf(scr + S_BETA + r * 4);
-                            stsf(scr + S_AM + r * A_LD + j * 4, j < r ? acc[nt][i] * br : 0.f);
+                            acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
                         }
+                    Frag16 T;
+                    unit_lower_inverse(acc, T, g, t);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 8 * nt + 2 * t;
+                        const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            SM_AT(uint32_t, pslot + P_TT + (g + 8 * hh) * SM_LD + col * 2) =
+                                pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
+                    }
                 } else {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int r = g + 8 * hh, j = 8 * nt + 2 * t;
-                            const float v0 = j <= r ? acc[nt][2 * hh] : 0.f;
-                            const float v1 = j + 1 <= r ? acc[nt][2 * hh + 1] : 0.f;
-                            sts32(pslot + P_PP + r * SM_LD + j * 2, pack_f16(v0, v1));
+                            const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
+                            const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
+                            SM_AT(uint32_t, pslot + P_PP + r * SM_LD + j * 2) = pack_f16(v0, v1);
                         }
                 }
-            }
-            named_bar_sync(bar_id, 64);
-
-            // T = (I + A)^-1 by forward substitution; lane c (mod 16) owns column c
-            if (lw == 0) {
-                const int c = lane & 15;
-                float tc[CHUNK];
-#pragma unroll
-                for (int r = 0; r < CHUNK; ++r) {
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                    for (int j4 = 0; j4 < r; j4 += 4) {
-                        const float4 a = ldsf4(scr + S_AM + r * A_LD + j4 * 4);
-                        if (j4 + 0 < r) s0 = fmaf(a.x, tc[j4 + 0], s0);
-                        if (j4 + 1 < r) s1 = fmaf(a.y, tc[j4 + 1], s1);
-                        if (j4 + 2 < r) s2 = fmaf(a.z, tc[j4 + 2], s2);
-                        if (j4 + 3 < r) s3 = fmaf(a.w, tc[j4 + 3], s3);
-                    }
-                    tc[r] = (r == c ? 1.f : 0.f) - ((s0 + s1) + (s2 + s3));
-                }
-                const float bc = ldsf(scr + S_BETA + c * 4);
-#pragma unroll
-                for (int j = 0; j < CHUNK; ++j)
-                    if ((j >> 3) == (lane >> 4)) sts16(pslot + P_TT + j * SM_LD + c * 2, f2h_bits(tc[j] * bc));
             }
             const bool stop = named_bar_or(bar_id, 64, failed);
             if (lt == 0) mbar_arrive(prep_full + 8 * ln);
@@ -318,7 +308,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int j = 8 * nt + 2 * t + (i & 1), vr = vr0 + g + 8 * (i >> 1);
-                const float vv = j < Lv ? __uint_as_float(static_cast<uint32_t>(lds16(vt + raw_off(j, vr))) << 16) : 0.f;
+                const float vv = j < Lv ? __uint_as_float(static_cast<uint32_t>(SM_AT(const uint16_t, vt + raw_off(j, vr))) << 16) : 0.f;
                 R[nt][i] = vv - z[nt][i];
             }
         __syncwarp();
@@ -332,7 +322,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
         for (int nt = 0; nt < 2; ++nt) {
             e[nt][0] = e[nt][1] = e[nt][2] = e[nt][3] = 0.f;
             const uint32_t row = pb + P_TT + (8 * nt + g) * SM_LD + 4 * t;
-            mma_f16(e[nt], ra, lds32(row), lds32(row + 16));
+            mma_f16(e[nt], ra, SM_AT(const uint32_t, row), SM_AT(const uint32_t, row + 16));
         }
         const uint32_t ea[4] = {pack_f16(e[0][0], e[0][1]), pack_f16(e[0][2], e[0][3]), pack_f16(e[1][0], e[1][1]),
                                 pack_f16(e[1][2], e[1][3])};
@@ -341,7 +331,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const uint32_t row = pb + P_PP + (8 * nt + g) * SM_LD + 4 * t;
-            mma_f16(z[2 + nt], ea, lds32(row), lds32(row + 16));
+            mma_f16(z[2 + nt], ea, SM_AT(const uint32_t, row), SM_AT(const uint32_t, row + 16));
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -354,7 +344,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
         // S = S Diag(gamma) + E Kbar
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
-            const float2 gm = ldsf2(pb + P_GAM + (8 * nt + 2 * t) * 4);
+            const float2 gm = SM_AT(const float2, pb + P_GAM + (8 * nt + 2 * t) * 4);
             S[nt][0] *= gm.x;
             S[nt][1] *= gm.y;
             S[nt][2] *= gm.x;
@@ -386,6 +376,8 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
     }
 }
 
+
+#undef SM_AT
 
 }  // namespace v1
 }  // namespace kda

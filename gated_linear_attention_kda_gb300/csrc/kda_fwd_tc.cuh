@@ -39,6 +39,7 @@
 // Inversion"), tensor contract ("FlashKDA Input Tensor Shapes and DTypes ...").
 #pragma once
 #include "kda_common.cuh"
+#include "kda_chunk.cuh"
 #include "tcgen05.cuh"
 
 namespace kda {
@@ -64,16 +65,16 @@ constexpr int L_CP = 18432;    // f16 C'_{n-2}^T [32 n][16 k]
 constexpr int L_GAM = 19456;   // fp32 gamma [128]
 constexpr int SLOT = 20480;
 
-// prep scratch (per lane)
-constexpr int F_LD = 528;  // fp32 [16][132]
-constexpr int A_LD = 80;   // fp32 [16][20]
-constexpr int H_LD = 272;  // f16 [16][136]
-constexpr int M_LD = 48;   // f16 [16][24]
-constexpr int S_KL = 0;
-constexpr int S_QL = 16 * F_LD;
-constexpr int S_KR = 32 * F_LD;
-constexpr int S_AM = 48 * F_LD;
-constexpr int S_BETA = S_AM + 16 * A_LD;
+// prep scratch (per lane); 16-bit tiles are [16][136] (272-byte rows)
+constexpr int H_LD = 272;
+constexpr int M_LD = 48;   // 16-bit [16][24]
+constexpr int S_KLH = 0;   // bf16 hi/lo of K * 2^(G - G_mid), Q * 2^(G - G_mid), K * 2^(G_mid - G)
+constexpr int S_KLL = S_KLH + 16 * H_LD;
+constexpr int S_QLH = S_KLL + 16 * H_LD;
+constexpr int S_QLL = S_QLH + 16 * H_LD;
+constexpr int S_KRH = S_QLL + 16 * H_LD;
+constexpr int S_KRL = S_KRH + 16 * H_LD;
+constexpr int S_BETA = S_KRL + 16 * H_LD;
 constexpr int S_KG = S_BETA + 64;
 constexpr int S_QG = S_KG + 16 * H_LD;
 constexpr int S_TP = S_QG + 16 * H_LD;
@@ -115,8 +116,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
 {
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    // align to 1024 B by pointer arithmetic on the shared array, so that accesses
+    // through `smem` stay in the shared address space
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
+// plain C++ shared-memory access at a 32-bit shared address (lets the compiler schedule it)
+#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seq = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const Span sp = seq_span(p, seq);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    const float4 gv = ldsf4(gam + (32 * g4 + i) * 4);
+                    const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
                     const float a0 = __uint_as_float(r32[i]) * gv.x, a1 = __uint_as_float(r32[i + 1]) * gv.y;
                     const float a2 = __uint_as_float(r32[i + 2]) * gv.z, a3 = __uint_as_float(r32[i + 3]) * gv.w;
                     r32[i] = __float_as_uint(a0);
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
                 for (int r = 0; r < CHUNK; ++r) {
-                    const uint32_t gw = lds32(raw + OFF_G + raw_off(r, c0));
+                    const uint32_t gw = SM_AT(const uint32_t, raw + OFF_G + raw_off(r, c0));
                     const float x0 = a_h * (bf16_lo(gw) + bias0), x1 = a_h * (bf16_hi(gw) + bias1);
                     const float ga0 = fmaf(hs, tanh_approx(0.5f * x0), hs);
                     const float ga1 = fmaf(hs, tanh_approx(0.5f * x1), hs);
@@ -419,15 +424,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
 
             const float Gm0 = G0[7], Gm1 = G1[7];
-            const float sm0 = ex2_approx(-Gm0) * TRUNC_COMP, sm1 = ex2_approx(-Gm1) * TRUNC_COMP;
+            const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
             const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
-            stsf2(sl + L_GAM + c0 * 4, ex2_approx(G0[15]), ex2_approx(G1[15]));
+            SM_AT(float2, sl + L_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
             float kb0[CHUNK], kb1[CHUNK];
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
-                const uint32_t kw = lds32(raw + OFF_K + raw_off(r, c0));
-                const uint32_t qw = lds32(raw + OFF_Q + raw_off(r, c0));
-                const uint32_t vw = lds32(raw + OFF_V + raw_off(r, c0));
+                const uint32_t kw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
+                const uint32_t qw = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
+                const uint32_t vw = SM_AT(const uint32_t, raw + OFF_V + raw_off(r, c0));
                 const bool live = r < Lv;
                 const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
                 const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
@@ -435,13 +440,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);
                 const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);
                 const float kg0 = k0 * gm0, kg1 = k1 * gm1, qg0 = q0 * gm0, qg1 = q1 * gm1;
-                sts32(scr + S_KG + r * H_LD + c0 * 2, pack_f16(kg0, kg1));
-                sts32(scr + S_QG + r * H_LD + c0 * 2, pack_f16(qg0, qg1));
-                sts32(sl + L_V16 + raw_off(r, c0), pack_f16(v0, v1));
-                stsf2(scr + S_KL + r * F_LD + c0 * 4, kg0 * sm0, kg1 * sm1);
-                stsf2(scr + S_QL + r * F_LD + c0 * 4, qg0 * sm0, qg1 * sm1);
+                SM_AT(uint32_t, scr + S_KG + r * H_LD + c0 * 2) = pack_f16(kg0, kg1);
+                SM_AT(uint32_t, scr + S_QG + r * H_LD + c0 * 2) = pack_f16(qg0, qg1);
+                SM_AT(uint32_t, sl + L_V16 + raw_off(r, c0)) = pack_f16(v0, v1);
                 const float kr0 = k0 * f0, kr1 = k1 * f1;
-                stsf2(scr + S_KR + r * F_LD + c0 * 4, kr0 * TRUNC_COMP, kr1 * TRUNC_COMP);
+                {
+                    const uint32_t o = r * H_LD + c0 * 2;
+                    uint32_t hi, lo;
+                    split_bf16(kg0 * sm0, kg1 * sm1, hi, lo);
+                    SM_AT(uint32_t, scr + S_KLH + o) = hi;
+                    SM_AT(uint32_t, scr + S_KLL + o) = lo;
+                    split_bf16(qg0 * sm0, qg1 * sm1, hi, lo);
+                    SM_AT(uint32_t, scr + S_QLH + o) = hi;
+                    SM_AT(uint32_t, scr + S_QLL + o) = lo;
+                    split_bf16(kr0, kr1, hi, lo);
+                    SM_AT(uint32_t, scr + S_KRH + o) = hi;
+                    SM_AT(uint32_t, scr + S_KRL + o) = lo;
+                }
                 kb0[r] = kr0 * se0;
                 kb1[r] = kr1 * se1;
             }
@@ -453,82 +468,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     w1[i] = pack_f16(kb1[2 * i], kb1[2 * i + 1]);
                 }
                 const uint32_t a0 = sl + L_KB + cm16(c0, 0), a1 = sl + L_KB + cm16(c0 + 1, 0);
-                sts128(a0, w0[0], w0[1], w0[2], w0[3]);
-                sts128(a0 + 128, w0[4], w0[5], w0[6], w0[7]);
-                sts128(a1, w1[0], w1[1], w1[2], w1[3]);
-                sts128(a1 + 128, w1[4], w1[5], w1[6], w1[7]);
+                SM_AT(uint4, a0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+                SM_AT(uint4, a0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+                SM_AT(uint4, a1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                SM_AT(uint4, a1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
             }
             if (lw == 1 && lane < CHUNK)
-                stsf(scr + S_BETA + lane * 4, lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f);
+                SM_AT(float, scr + S_BETA + lane * 4) = lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
             named_bar_sync(bar_id, 64);
             if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
 
-            // A (warp 0) and P (warp 1), tf32
+            // warp 0: A = strictly-lower(beta_r Kl Kr^T) and T' = (I + A)^-1 diag(beta);
+            // warp 1: P = lower(Ql Kr^T). Three bf16 products per entry (hi/lo split).
             {
-                const uint32_t X = scr + (lw == 0 ? S_KL : S_QL);
-                float acc[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const int cc = 8 * ks + t;
-                    const float a0 = ldsf(X + g * F_LD + cc * 4), a1 = ldsf(X + (g + 8) * F_LD + cc * 4);
-                    const float a2 = ldsf(X + g * F_LD + (cc + 4) * 4), a3 = ldsf(X + (g + 8) * F_LD + (cc + 4) * 4);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const float b0 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + cc * 4);
-                        const float b1 = ldsf(scr + S_KR + (8 * nt + g) * F_LD + (cc + 4) * 4);
-                        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
-                    }
-                }
+                Frag16 acc;
+                if (lw == 0)
+                    chunk_gram_x3(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane);
+                else
+                    chunk_gram_x3(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane);
                 if (lw == 0) {
+                    const float bg = SM_AT(const float, scr + S_BETA + g * 4), bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
-                            const float br = ldsf(scr + S_BETA + r * 4);
-                            stsf(scr + S_AM + r * A_LD + j * 4, j < r ? acc[nt][i] * br : 0.f);
+                            acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
                         }
+                    Frag16 T;
+                    unit_lower_inverse(acc, T, g, t);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 8 * nt + 2 * t;
+                        const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh;
+                            const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
+                            SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
+                            SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
+                        }
+                    }
                 } else {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int r = g + 8 * hh, j = 8 * nt + 2 * t;
-                            const float v0 = j <= r ? acc[nt][2 * hh] : 0.f;
-                            const float v1 = j + 1 <= r ? acc[nt][2 * hh + 1] : 0.f;
-                            sts32(scr + S_PP + r * M_LD + j * 2, pack_f16(v0, v1));
+                            const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
+                            const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
+                            SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
                         }
                 }
-            }
-            named_bar_sync(bar_id, 64);
-
-            // T' = (I + A)^-1 diag(beta) by forward substitution (warp 0); lane c (mod 16) owns column c
-            if (lw == 0) {
-                const int c = lane & 15;
-                float tc_[CHUNK];
-#pragma unroll
-                for (int r = 0; r < CHUNK; ++r) {
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                    for (int j4 = 0; j4 < r; j4 += 4) {
-                        const float4 a = ldsf4(scr + S_AM + r * A_LD + j4 * 4);
-                        if (j4 + 0 < r) s0 = fmaf(a.x, tc_[j4 + 0], s0);
-                        if (j4 + 1 < r) s1 = fmaf(a.y, tc_[j4 + 1], s1);
-                        if (j4 + 2 < r) s2 = fmaf(a.z, tc_[j4 + 2], s2);
-                        if (j4 + 3 < r) s3 = fmaf(a.w, tc_[j4 + 3], s3);
-                    }
-                    tc_[r] = (r == c ? 1.f : 0.f) - ((s0 + s1) + (s2 + s3));
-                }
-                const float bc = ldsf(scr + S_BETA + c * 4);
-#pragma unroll
-                for (int j = 0; j < CHUNK; ++j)
-                    if ((j >> 3) == (lane >> 4)) {
-                        const uint16_t hv = f2h_bits(tc_[j] * bc);
-                        sts16(scr + S_TP + j * M_LD + c * 2, hv);
-                        sts16(sl + L_TM + cm16(j, c), hv);
-                    }
             }
             named_bar_sync(bar_id, 64);
 
@@ -557,7 +548,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             const int r = g + 8 * hh, col = 8 * nt + 2 * t;
-                            sts32(sl + L_TM + cm16(16 + r, col), pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]));
+                            SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
                         }
                     aX[0] = pack_f16(-sc * m[0][0], -sc * m[0][1]);
                     aX[1] = pack_f16(-sc * m[0][2], -sc * m[0][3]);
@@ -606,11 +597,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int nt = 2 * kk + half, c = 8 * nt + 2 * t;
-                    const float2 gv = n >= 1 ? ldsf2(prev + L_GAM + c * 4) : make_float2(1.f, 1.f);
+                    const float2 gv = n >= 1 ? SM_AT(const float2, prev + L_GAM + c * 4) : make_float2(1.f, 1.f);
                     const float y0 = acc[nt][0] * gv.x, y1 = acc[nt][1] * gv.y;
                     const float y2 = acc[nt][2] * gv.x, y3 = acc[nt][3] * gv.y;
-                    sts32(sl + L_WY + sw128_32rows(rowA, c), pack_bf16(y0, y1));
-                    sts32(sl + L_WY + sw128_32rows(rowA + 8, c), pack_bf16(y2, y3));
+                    SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA, c)) = pack_bf16(y0, y1);
+                    SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA + 8, c)) = pack_bf16(y2, y3);
                     bx[0][half] = pack_f16(acc[nt][0], acc[nt][1]);
                     bx[1][half] = pack_f16(acc[nt][2], acc[nt][3]);
                     by[0][half] = pack_f16(y0, y1);
@@ -636,8 +627,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int j = g + 8 * (i >> 1), col = 16 * lw + 8 * nu + 2 * t + (i & 1);
-                    if (n >= 1) sts16(sl + L_CC + cm16(col, j), f2h_bits(cacc[nu][i]));
-                    if (n >= 2) sts16(sl + L_CP + cm16(col, j), f2h_bits(pacc[nu][i]));
+                    if (n >= 1) SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cacc[nu][i]);
+                    if (n >= 2) SM_AT(uint16_t, sl + L_CP + cm16(col, j)) = f2h_bits(pacc[nu][i]);
                 }
             tc::fence_async_smem();
             const bool stop = named_bar_or(bar_id, 64, failed);
@@ -655,6 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
     }
+#undef SM_AT
 }
 
 }  // namespace tcs
