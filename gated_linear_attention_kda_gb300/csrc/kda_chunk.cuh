@@ -73,32 +73,32 @@ __device__ __forceinline__ void frag_mul(Frag16 &c, const uint32_t (&a)[4], cons
 // as (I - A)(I + A^2)(I + A^4)(I + A^8) with f16 operands.
 __device__ __forceinline__ void unit_lower_inverse(const Frag16 &A, Frag16 &T, int g, int t)
 {
-    uint32_t a[4], b[2][2];
-    Frag16 p2, p4, p8, m;
+    uint32_t a[4], b[2][2], ax[4], bx[2][2];
+    Frag16 p2, p4, p8, m, x;
     frag_as_a(A, a);
     frag_as_b(A, b);
     frag_mul(p2, a, b);            // A^2
-    frag_as_a(p2, a);
-    frag_as_b(p2, b);
-    frag_mul(p4, a, b);            // A^4
-    frag_as_a(p4, a);
-    frag_as_b(p4, b);
-    frag_mul(p8, a, b);            // A^8
-    Frag16 x = A;                  // I - A
+    Frag16 ia = A;                 // I - A
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x.c[nt][i] = -x.c[nt][i];
-    frag_add_diag(x, 1.f, g, t);
-    frag_add_diag(p2, 1.f, g, t);
-    frag_add_diag(p4, 1.f, g, t);
-    frag_add_diag(p8, 1.f, g, t);
-    frag_as_a(x, a);
+        for (int i = 0; i < 4; ++i) ia.c[nt][i] = -ia.c[nt][i];
+    frag_add_diag(ia, 1.f, g, t);
+    frag_as_a(p2, a);
     frag_as_b(p2, b);
-    frag_mul(m, a, b);             // (I - A)(I + A^2)
-    frag_as_a(m, a);
+    frag_mul(p4, a, b);            // A^4
+    frag_add_diag(p2, 1.f, g, t);
+    frag_as_a(ia, ax);
+    frag_as_b(p2, bx);
+    frag_mul(m, ax, bx);           // (I - A)(I + A^2), independent of A^4
+    frag_as_a(p4, a);
     frag_as_b(p4, b);
-    frag_mul(x, a, b);             // ... (I + A^4)
+    frag_mul(p8, a, b);            // A^8
+    frag_add_diag(p4, 1.f, g, t);
+    frag_as_a(m, ax);
+    frag_as_b(p4, bx);
+    frag_mul(x, ax, bx);           // ... (I + A^4), independent of A^8
+    frag_add_diag(p8, 1.f, g, t);
     frag_as_a(x, a);
     frag_as_b(p8, b);
     frag_mul(T, a, b);             // ... (I + A^8)
@@ -111,20 +111,33 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
     lo = pack_bf16(x0 - bf16_lo(hi), x1 - bf16_hi(hi));
 }
 
-// acc[nt] (16 rows r x 16 cols j) = sum_c X[r][c] R[j][c] from bf16 hi/lo tiles
-// stored row-major [16][136] (272-byte rows): three bf16 products
-// Xh Rh + Xh Rl + Xl Rh give ~16-bit operand precision with a bf16 exponent range.
+// Split two floats into a truncated bf16 hi part and a rounded bf16 lo part
+// (x ~= hi + lo to ~16 mantissa bits); hi is a byte permute, x - hi is exact.
+__device__ __forceinline__ void split_bf16_trunc(float x0, float x1, uint32_t &hi, uint32_t &lo)
+{
+    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+    hi = __byte_perm(b0, b1, 0x7632);
+    lo = pack_bf16(x0 - __uint_as_float(b0 & 0xffff0000u), x1 - __uint_as_float(b1 & 0xffff0000u));
+}
+
+// acc[nt] (16 rows r x 16 cols j) = sum_c X[r][c] R[j][c] over the channels
+// c in [16 kbase, 16 (kbase + NK)), from bf16 hi/lo tiles stored row-major
+// [16][136] (272-byte rows): three bf16 products Xh Rh + Xh Rl + Xl Rh give
+// ~16-bit operand precision with a bf16 exponent range.
+template <int NK>
 __device__ __forceinline__ void chunk_gram_x3(uint32_t xh, uint32_t xl, uint32_t rh, uint32_t rl, Frag16 &acc,
-                                              int lane)
+                                              int lane, int kbase)
 {
     const int mi = lane >> 3, ri = lane & 7;
     // A operand: rows r = ri + 8 (mi & 1), cols 16 kk + 8 (mi >> 1)
-    const uint32_t aoff = (ri + 8 * (mi & 1)) * 272 + 16 * (mi >> 1);
+    const uint32_t aoff = (ri + 8 * (mi & 1)) * 272 + 16 * (mi >> 1) + 32 * kbase;
     // B operand (rows j, K = c contiguous): n-tile = mi >> 1, k half = mi & 1
-    const uint32_t boff = (ri + 8 * (mi >> 1)) * 272 + 16 * (mi & 1);
+    const uint32_t boff = (ri + 8 * (mi >> 1)) * 272 + 16 * (mi & 1) + 32 * kbase;
+    Frag16 cross;
     frag_zero(acc);
+    frag_zero(cross);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < NK; ++kk) {
         uint32_t ah[4], al[4], bh[4], bl[4];
         ldsm_x4(xh + aoff + 32 * kk, ah[0], ah[1], ah[2], ah[3]);
         ldsm_x4(xl + aoff + 32 * kk, al[0], al[1], al[2], al[3]);
@@ -132,11 +145,15 @@ __device__ __forceinline__ void chunk_gram_x3(uint32_t xh, uint32_t xl, uint32_t
         ldsm_x4(rl + boff + 32 * kk, bl[0], bl[1], bl[2], bl[3]);
         mma_bf16(acc.c[0], ah, bh[0], bh[1]);
         mma_bf16(acc.c[1], ah, bh[2], bh[3]);
-        mma_bf16(acc.c[0], ah, bl[0], bl[1]);
-        mma_bf16(acc.c[1], ah, bl[2], bl[3]);
-        mma_bf16(acc.c[0], al, bh[0], bh[1]);
-        mma_bf16(acc.c[1], al, bh[2], bh[3]);
+        mma_bf16(cross.c[0], ah, bl[0], bl[1]);
+        mma_bf16(cross.c[1], ah, bl[2], bl[3]);
+        mma_bf16(cross.c[0], al, bh[0], bh[1]);
+        mma_bf16(cross.c[1], al, bh[2], bh[3]);
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc.c[nt][i] += cross.c[nt][i];
 }
 
 }  // namespace kda

@@ -166,10 +166,16 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
             const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
             const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
             SM_AT(float2, pslot + P_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
+            // all raw loads first: stores below may alias them as far as the compiler knows
+            uint32_t kwv[CHUNK], qwv[CHUNK];
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
-                const uint32_t kw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
-                const uint32_t qw = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
+                kwv[r] = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
+                qwv[r] = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
+            }
+#pragma unroll
+            for (int r = 0; r < CHUNK; ++r) {
+                const uint32_t kw = kwv[r], qw = qwv[r];
                 const bool live = r < Lv;
                 const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
                 const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
@@ -201,9 +207,9 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
             {
                 Frag16 acc;
                 if (lw == 0)
-                    chunk_gram_x3(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane);
+                    chunk_gram_x3<8>(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane, 0);
                 else
-                    chunk_gram_x3(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane);
+                    chunk_gram_x3<8>(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane, 0);
                 if (lw == 0) {
                     const float bg = SM_AT(const float, scr + S_BETA + g * 4), bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll

@@ -21,13 +21,13 @@
 // Only the last term depends on the previous chunk's result, so each chunk's
 // critical path is one 16-deep MMA plus one commit.
 //
-// Warp roles (320 threads):
+// Warp roles (448 threads):
 //   warp 0      TMA producer (lane 0); allocates / frees tensor memory.
 //   warp 1      MMA issuer (lane 0).
 //   warps 2-5   state warps, one V row per thread (tensor-memory lane):
 //               read [E|O], hand E to the tensor core, decay the state
 //               (S <- S Diag(gamma)) and keep its bf16 copy, store outputs.
-//   warps 6-9   two prep lanes of two warps, alternate chunks.
+//   warps 6-13  two prep lanes of four warps, alternate chunks.
 // Tensor memory (512 columns): state fp32 [0,128), D x3 [128,224),
 // E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384).
 //
@@ -47,7 +47,7 @@ namespace tcs {
 
 constexpr int NR = 4;  // raw chunk ring
 constexpr int NP = 4;  // prep slot ring
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 448;
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;     // fp32 state, 128 columns
@@ -74,12 +74,14 @@ constexpr int S_QLH = S_KLL + 16 * H_LD;
 constexpr int S_QLL = S_QLH + 16 * H_LD;
 constexpr int S_KRH = S_QLL + 16 * H_LD;
 constexpr int S_KRL = S_KRH + 16 * H_LD;
-constexpr int S_BETA = S_KRL + 16 * H_LD;
-constexpr int S_KG = S_BETA + 64;
-constexpr int S_QG = S_KG + 16 * H_LD;
-constexpr int S_TP = S_QG + 16 * H_LD;
-constexpr int S_PP = S_TP + 16 * M_LD;
-constexpr int SCR = S_PP + 16 * M_LD;
+constexpr int S_KG = S_KRL + 16 * H_LD;  // f16 K * Gamma
+constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
+constexpr int S_TP = S_QG + 16 * H_LD;   // f16 T' [16][24]
+constexpr int S_PP = S_TP + 16 * M_LD;   // f16 P [16][24]
+constexpr int S_BETA = S_PP + 16 * M_LD; // fp32 beta [16]
+constexpr int S_GX = S_BETA + 64;        // fp32x2 [2 halves][64 pairs]: gate sums exchanged between row halves
+constexpr int S_AX = S_GX + 1024;        // fp32 [2][2][32 lanes][4]: second channel half of A and P
+constexpr int SCR = S_AX + 2048;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_SLOT = OFF_RAW + NR * RAW_STAGE;
@@ -94,7 +96,7 @@ constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 
 static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0, "swizzled operands need 1024-byte alignment");
-static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && SCR % 16 == 0, "ldmatrix alignment");
+static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && S_AX % 16 == 0 && SCR % 16 == 0, "alignment");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -316,11 +318,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tc::fence_after();
             const uint32_t gam = slot(k) + L_GAM;
-#pragma unroll 1
-            for (int g4 = 0; g4 < 4; ++g4) {
-                uint32_t r32[32], r16[16];
-                tc::ld32(lb + T_S + 32 * g4, r32);
-                tc::wait_ld();
+            // four 32-column blocks, the next block's load in flight while one is decayed
+            auto decay_block = [&](int g4, uint32_t(&r32)[32]) {
+                uint32_t r16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
@@ -335,6 +335,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tc::st32(lb + T_S + 32 * g4, r32);
                 tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);
+            };
+            {
+                uint32_t ra[32], rb[32];
+                tc::ld32(lb + T_S, ra);
+                tc::wait_ld();
+                tc::ld32(lb + T_S + 32, rb);
+                decay_block(0, ra);
+                tc::wait_ld();
+                tc::ld32(lb + T_S + 64, ra);
+                decay_block(1, rb);
+                tc::wait_ld();
+                tc::ld32(lb + T_S + 96, rb);
+                decay_block(2, ra);
+                tc::wait_ld();
+                decay_block(3, rb);
             }
             tc::wait_st();
             tc::fence_before();
@@ -377,17 +392,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::fence_before();
     } else {
         // ---------------------------------------------------------------- prep lanes
-        const int ln = (warp - 6) >> 1;
-        const int lt = threadIdx.x - 192 - 64 * ln;  // 0..63
+        // lane = 4 warps = 128 threads. Element-wise passes: thread -> channel pair
+        // (c0, c0 + 1), rows [8 rh, 8 rh + 8). Products: warp lw, row block
+        // wrow = lw >> 1 of WX (0: -w, 1: s q^), channel half chalf = lw & 1.
+        const int ln = (warp - 6) >> 2;
+        const int lt = threadIdx.x - 192 - 128 * ln;  // 0..127
         const int lw = lt >> 5;
         const uint32_t bar_id = 1 + ln;
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
-        const int c0 = 2 * lt;
-        float a_h = 1.f, bias0 = 0.f, bias1 = 0.f;
-        if (p.A_log) a_h = ex2_approx(__ldg(p.A_log + h) * LOG2E);
+        const int cp = lt & 63, rh = lt >> 6;
+        const int c0 = 2 * cp, r0 = 8 * rh;
+        const int wrow = lw >> 1, chalf = lw & 1;
+        // x / 2 = ah2 * g + bb, with x = exp(A_log) (g + dt_bias)
+        float ah2 = 0.5f, bb0 = 0.f, bb1 = 0.f;
+        if (p.A_log) ah2 = 0.5f * ex2_approx(__ldg(p.A_log + h) * LOG2E);
         if (p.dt_bias) {
-            bias0 = __ldg(p.dt_bias + h * DH + c0);
-            bias1 = __ldg(p.dt_bias + h * DH + c0 + 1);
+            bb0 = ah2 * __ldg(p.dt_bias + h * DH + c0);
+            bb1 = ah2 * __ldg(p.dt_bias + h * DH + c0 + 1);
         }
         const float hs = p.half_gs, sc = p.scale;
         const int g = lane >> 2, t = lane & 3;
@@ -400,141 +421,161 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int tok0 = sp.bos + n * CHUNK;
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
             float blogit = 0.f;
-            if (lw == 1 && lane < Lv)
-                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lane) * p.H + h)) << 16);
+            if (lt < Lv)
+                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lt) * p.H + h)) << 16);
             if (!wait_bar(bar(B_RAW_FULL + rs), (n / NR) & 1, flags)) failed = true;
             const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
 
-            // gate (log2 units) and its inclusive in-chunk cumsum
-            float G0[CHUNK], G1[CHUNK];
+            // gate (log2 units) over this thread's 8 rows, local inclusive cumsum;
+            // rows past the chunk's end add nothing
+            float G0[8], G1[8];
             {
-                float acc0 = 0.f, acc1 = 0.f;
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int r = 0; r < CHUNK; ++r) {
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + i;
                     const uint32_t gw = SM_AT(const uint32_t, raw + OFF_G + raw_off(r, c0));
-                    const float x0 = a_h * (bf16_lo(gw) + bias0), x1 = a_h * (bf16_hi(gw) + bias1);
-                    const float ga0 = fmaf(hs, tanh_approx(0.5f * x0), hs);
-                    const float ga1 = fmaf(hs, tanh_approx(0.5f * x1), hs);
-                    acc0 += (r < Lv) ? ga0 : 0.f;
-                    acc1 += (r < Lv) ? ga1 : 0.f;
-                    G0[r] = acc0;
-                    G1[r] = acc1;
+                    const float t0 = tanh_approx(fmaf(ah2, bf16_lo(gw), bb0));
+                    const float t1 = tanh_approx(fmaf(ah2, bf16_hi(gw), bb1));
+                    const bool live = r < Lv;
+                    a0 += live ? fmaf(hs, t0, hs) : 0.f;
+                    a1 += live ? fmaf(hs, t1, hs) : 0.f;
+                    G0[i] = a0;
+                    G1[i] = a1;
                 }
             }
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
-
-            const float Gm0 = G0[7], Gm1 = G1[7];
-            const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
-            const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
-            SM_AT(float2, sl + L_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
-            float kb0[CHUNK], kb1[CHUNK];
+            SM_AT(float2, scr + S_GX + rh * 512 + cp * 8) = make_float2(G0[7], G1[7]);
+            if (lt < CHUNK)
+                SM_AT(float, scr + S_BETA + lt * 4) = lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
+            named_bar_sync(bar_id, 128);
+            // Gm = G at row 7 (reference: halves the exponent range), Ge = G at row 15;
+            // d = G_r - Gm for this thread's rows
+            const float2 oth = SM_AT(const float2, scr + S_GX + (rh ^ 1) * 512 + cp * 8);
+            const float Gm0 = rh ? oth.x : G0[7], Gm1 = rh ? oth.y : G1[7];
+            const float Ge0 = rh ? oth.x + G0[7] : G0[7] + oth.x, Ge1 = rh ? oth.y + G1[7] : G1[7] + oth.y;
+            const float off0 = rh ? 0.f : Gm0, off1 = rh ? 0.f : Gm1;
+            const float gr0 = ex2_approx(Gm0), gr1 = ex2_approx(Gm1);            // 2^Gm
+            const float se0 = ex2_approx(Ge0 - Gm0), se1 = ex2_approx(Ge1 - Gm1);  // 2^(Ge - Gm)
+            if (rh) SM_AT(float2, sl + L_GAM + c0 * 4) = make_float2(ex2_approx(Ge0), ex2_approx(Ge1));
+            // all raw loads first: stores below may alias them as far as the compiler knows
+            uint32_t kwv[8], qwv[8], vwv[8];
 #pragma unroll
-            for (int r = 0; r < CHUNK; ++r) {
-                const uint32_t kw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
-                const uint32_t qw = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
-                const uint32_t vw = SM_AT(const uint32_t, raw + OFF_V + raw_off(r, c0));
-                const bool live = r < Lv;
-                const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
-                const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
-                const float v0 = live ? bf16_lo(vw) : 0.f, v1 = live ? bf16_hi(vw) : 0.f;
-                const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);
-                const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);
-                const float kg0 = k0 * gm0, kg1 = k1 * gm1, qg0 = q0 * gm0, qg1 = q1 * gm1;
-                SM_AT(uint32_t, scr + S_KG + r * H_LD + c0 * 2) = pack_f16(kg0, kg1);
-                SM_AT(uint32_t, scr + S_QG + r * H_LD + c0 * 2) = pack_f16(qg0, qg1);
-                SM_AT(uint32_t, sl + L_V16 + raw_off(r, c0)) = pack_f16(v0, v1);
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + i;
+                const uint32_t kraw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
+                kwv[i] = r < Lv ? kraw : 0u;  // keys past the chunk's end are zero
+                qwv[i] = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
+                vwv[i] = SM_AT(const uint32_t, raw + OFF_V + raw_off(r, c0));
+            }
+            float kb0[8], kb1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + i;
+                const uint32_t kw = kwv[i], qw = qwv[i], vw = vwv[i];
+                const float d0 = G0[i] - off0, d1 = G1[i] - off1;
+                const float u0 = ex2_approx(d0), u1 = ex2_approx(d1);     // 2^(G_r - Gm)
+                const float f0 = ex2_approx(-d0), f1 = ex2_approx(-d1);   // 2^(Gm - G_r)
+                const float k0 = bf16_lo(kw), k1 = bf16_hi(kw), q0 = bf16_lo(qw), q1 = bf16_hi(qw);
+                const float kl0 = k0 * u0, kl1 = k1 * u1, ql0 = q0 * u0, ql1 = q1 * u1;
                 const float kr0 = k0 * f0, kr1 = k1 * f1;
-                {
-                    const uint32_t o = r * H_LD + c0 * 2;
-                    uint32_t hi, lo;
-                    split_bf16(kg0 * sm0, kg1 * sm1, hi, lo);
-                    SM_AT(uint32_t, scr + S_KLH + o) = hi;
-                    SM_AT(uint32_t, scr + S_KLL + o) = lo;
-                    split_bf16(qg0 * sm0, qg1 * sm1, hi, lo);
-                    SM_AT(uint32_t, scr + S_QLH + o) = hi;
-                    SM_AT(uint32_t, scr + S_QLL + o) = lo;
-                    split_bf16(kr0, kr1, hi, lo);
-                    SM_AT(uint32_t, scr + S_KRH + o) = hi;
-                    SM_AT(uint32_t, scr + S_KRL + o) = lo;
-                }
-                kb0[r] = kr0 * se0;
-                kb1[r] = kr1 * se1;
+                const uint32_t o = r * H_LD + c0 * 2;
+                SM_AT(uint32_t, scr + S_KG + o) = pack_f16(kl0 * gr0, kl1 * gr1);  // K * Gamma
+                SM_AT(uint32_t, scr + S_QG + o) = pack_f16(ql0 * gr0, ql1 * gr1);  // Q * Gamma
+                SM_AT(uint32_t, sl + L_V16 + raw_off(r, c0)) = pack_f16(bf16_lo(vw), bf16_hi(vw));
+                uint32_t hi, lo;
+                split_bf16_trunc(kl0, kl1, hi, lo);
+                SM_AT(uint32_t, scr + S_KLH + o) = hi;
+                SM_AT(uint32_t, scr + S_KLL + o) = lo;
+                split_bf16_trunc(ql0, ql1, hi, lo);
+                SM_AT(uint32_t, scr + S_QLH + o) = hi;
+                SM_AT(uint32_t, scr + S_QLL + o) = lo;
+                split_bf16_trunc(kr0, kr1, hi, lo);
+                SM_AT(uint32_t, scr + S_KRH + o) = hi;
+                SM_AT(uint32_t, scr + S_KRL + o) = lo;
+                kb0[i] = kr0 * se0;
+                kb1[i] = kr1 * se1;
             }
-            {  // Kbar as the K-major [c][j] operand: two 16-byte rows per channel
-                uint32_t w0[8], w1[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    w0[i] = pack_f16(kb0[2 * i], kb0[2 * i + 1]);
-                    w1[i] = pack_f16(kb1[2 * i], kb1[2 * i + 1]);
-                }
-                const uint32_t a0 = sl + L_KB + cm16(c0, 0), a1 = sl + L_KB + cm16(c0 + 1, 0);
-                SM_AT(uint4, a0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-                SM_AT(uint4, a0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-                SM_AT(uint4, a1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                SM_AT(uint4, a1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-            }
-            if (lw == 1 && lane < CHUNK)
-                SM_AT(float, scr + S_BETA + lane * 4) = lane < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
-            named_bar_sync(bar_id, 64);
+            // Kbar = K * 2^(Ge - G_r) as the K-major [c][j] operand: one 16-byte row per channel
+            SM_AT(uint4, sl + L_KB + cm16(c0, r0)) = make_uint4(pack_f16(kb0[0], kb0[1]), pack_f16(kb0[2], kb0[3]),
+                                                               pack_f16(kb0[4], kb0[5]), pack_f16(kb0[6], kb0[7]));
+            SM_AT(uint4, sl + L_KB + cm16(c0 + 1, r0)) = make_uint4(pack_f16(kb1[0], kb1[1]), pack_f16(kb1[2], kb1[3]),
+                                                                   pack_f16(kb1[4], kb1[5]), pack_f16(kb1[6], kb1[7]));
+            named_bar_sync(bar_id, 128);
             if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
 
-            // warp 0: A = strictly-lower(beta_r Kl Kr^T) and T' = (I + A)^-1 diag(beta);
-            // warp 1: P = lower(Ql Kr^T). Three bf16 products per entry (hi/lo split).
+            // A (warps 0, 2) and P (warps 1, 3), each warp over one channel half;
+            // three bf16 products per entry (hi/lo split)
             {
+                const bool isP = lw & 1;
+                const int khalf = lw >> 1;
                 Frag16 acc;
-                if (lw == 0)
-                    chunk_gram_x3(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane);
-                else
-                    chunk_gram_x3(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane);
-                if (lw == 0) {
-                    const float bg = SM_AT(const float, scr + S_BETA + g * 4), bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
-                            acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
-                        }
-                    Frag16 T;
-                    unit_lower_inverse(acc, T, g, t);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int col = 8 * nt + 2 * t;
-                        const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = g + 8 * hh;
-                            const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
-                            SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
-                            SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = g + 8 * hh, j = 8 * nt + 2 * t;
-                            const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
-                            const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
-                            SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
-                        }
+                chunk_gram_x3<4>(scr + (isP ? S_QLH : S_KLH), scr + (isP ? S_QLL : S_KLL), scr + S_KRH, scr + S_KRL, acc,
+                                 lane, 4 * khalf);
+                const uint32_t xa = scr + S_AX + (isP ? 1024 : 0) + lane * 16;
+                if (khalf) {
+                    SM_AT(float4, xa) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
+                    SM_AT(float4, xa + 512) = make_float4(acc.c[1][0], acc.c[1][1], acc.c[1][2], acc.c[1][3]);
                 }
-            }
-            named_bar_sync(bar_id, 64);
-
-            // WX rows: warp 0 -> -w = -T' (K*Gamma); warp 1 -> s q^ = s (Q*Gamma) - s M (K*Gamma)
-            float acc[16][4];
+                named_bar_sync(bar_id, 128);
+                if (!khalf) {
+                    const float4 x0 = SM_AT(const float4, xa), x1 = SM_AT(const float4, xa + 512);
+                    acc.c[0][0] += x0.x; acc.c[0][1] += x0.y; acc.c[0][2] += x0.z; acc.c[0][3] += x0.w;
+                    acc.c[1][0] += x1.x; acc.c[1][1] += x1.y; acc.c[1][2] += x1.z; acc.c[1][3] += x1.w;
+                    if (!isP) {
+                        // A = strictly-lower, rows scaled by beta; T' = (I + A)^-1 diag(beta)
+                        const float bg = SM_AT(const float, scr + S_BETA + g * 4);
+                        const float bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
+                                acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
+                            }
+                        Frag16 T;
+                        unit_lower_inverse(acc, T, g, t);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int col = 8 * nt + 2 * t;
+                            const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int r = g + 8 * hh;
+                                const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
+                                SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
+                                SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
+                            }
+                        }
+                    } else {
+                        // P = lower (diagonal included)
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int r = g + 8 * hh, j = 8 * nt + 2 * t;
+                                const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
+                                const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
+                                SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
+                            }
+                    }
+                }
+                named_bar_sync(bar_id, 128);
+            }
+
+            // WX rows 16 wrow.. (0: -w = -T' (K*Gamma); 1: s q^ = s (Q*Gamma) - s M (K*Gamma)),
+            // channels 64 chalf..
+            float acc[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
             {
                 uint32_t aX[4];
-                if (lw == 0) {
+                if (wrow == 0) {
                     ldsm_x4(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aX[0], aX[1], aX[2], aX[3]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) aX[i] ^= 0x80008000u;
                 } else {
-                    // M = P T' (16 x 16 x 16); also TM rows 16..31 = s M
+                    // M = P T' (16 x 16 x 16); TM rows 16..31 = s M
                     uint32_t aP[4], b0, b1, b2, b3;
                     ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
                     ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
@@ -543,26 +584,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int i = 0; i < 2; ++i) m[i][0] = m[i][1] = m[i][2] = m[i][3] = 0.f;
                     mma_f16(m[0], aP, b0, b1);
                     mma_f16(m[1], aP, b2, b3);
+                    if (chalf == 0) {
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
+                        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = g + 8 * hh, col = 8 * nt + 2 * t;
-                            SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
-                        }
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int r = g + 8 * hh, col = 8 * nt + 2 * t;
+                                SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) =
+                                    pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
+                            }
+                    }
                     aX[0] = pack_f16(-sc * m[0][0], -sc * m[0][1]);
                     aX[1] = pack_f16(-sc * m[0][2], -sc * m[0][3]);
                     aX[2] = pack_f16(-sc * m[1][0], -sc * m[1][1]);
                     aX[3] = pack_f16(-sc * m[1][2], -sc * m[1][3]);
                 }
+                const uint32_t bkg = scr + S_KG + (ri + 8 * (mi & 1)) * H_LD + 128 * chalf + 16 * (mi >> 1);
 #pragma unroll
-                for (int m8 = 0; m8 < 8; ++m8) {
+                for (int m8 = 0; m8 < 4; ++m8) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(scr + S_KG + (ri + 8 * (mi & 1)) * H_LD + 32 * m8 + 16 * (mi >> 1), b0, b1, b2, b3);
+                    ldsm_x4_t(bkg + 32 * m8, b0, b1, b2, b3);
                     mma_f16(acc[2 * m8], aX, b0, b1);
                     mma_f16(acc[2 * m8 + 1], aX, b2, b3);
                 }
-                if (lw == 1) {
+                if (wrow == 1) {
                     // + s * I * (Q*Gamma)
                     const uint32_t sh = static_cast<uint32_t>(f2h_bits(sc));
                     uint32_t aI[4];
@@ -570,68 +615,93 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     aI[1] = 0u;
                     aI[2] = 0u;
                     aI[3] = aI[0];
+                    const uint32_t bqg = scr + S_QG + (ri + 8 * (mi & 1)) * H_LD + 128 * chalf + 16 * (mi >> 1);
 #pragma unroll
-                    for (int m8 = 0; m8 < 8; ++m8) {
+                    for (int m8 = 0; m8 < 4; ++m8) {
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(scr + S_QG + (ri + 8 * (mi & 1)) * H_LD + 32 * m8 + 16 * (mi >> 1), b0, b1, b2, b3);
+                        ldsm_x4_t(bqg + 32 * m8, b0, b1, b2, b3);
                         mma_f16(acc[2 * m8], aI, b0, b1);
                         mma_f16(acc[2 * m8 + 1], aI, b2, b3);
                     }
                 }
             }
 
-            // cross-chunk terms: gamma_{n-1}, Kbar_{n-1}, Kbar_{n-2}
+            // cross-chunk terms: gamma_{n-1}, Kbar_{n-1}, Kbar_{n-2}; partial sums over
+            // this warp's channel half
             if (n >= 1 && !wait_bar(bar(B_PREP_FULL + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
             const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
-            const int rowA = 16 * lw + g;
+            const int rowA = 16 * wrow + g;
             float cacc[2][4], pacc[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 cacc[i][0] = cacc[i][1] = cacc[i][2] = cacc[i][3] = 0.f;
                 pacc[i][0] = pacc[i][1] = pacc[i][2] = pacc[i][3] = 0.f;
             }
+            uint32_t wy[8][2];  // bf16 WY pairs, stored after the products
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                // WX / WY columns c in [16 kk, 16 kk + 16)
+            for (int kk = 0; kk < 4; ++kk) {
+                // WX / WY columns c in [64 chalf + 16 kk, +16)
+                const int kb = 4 * chalf + kk;
+                const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                // branch-free: for n < 2 the products read stale slots and are never stored / used
+                uint32_t aK1[4], aK2[4];
+                ldsm_x4_t(prev + L_KB + koff, aK1[0], aK1[1], aK1[2], aK1[3]);
+                ldsm_x4_t(prev2 + L_KB + koff, aK2[0], aK2[1], aK2[2], aK2[3]);
                 uint32_t bx[2][2], by[2][2];
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const int nt = 2 * kk + half, c = 8 * nt + 2 * t;
-                    const float2 gv = n >= 1 ? SM_AT(const float2, prev + L_GAM + c * 4) : make_float2(1.f, 1.f);
+                    const int nt = 2 * kk + half, c = 16 * kb + 8 * half + 2 * t;
+                    const float2 gl = SM_AT(const float2, prev + L_GAM + c * 4);
+                    const float2 gv = n >= 1 ? gl : make_float2(1.f, 1.f);
                     const float y0 = acc[nt][0] * gv.x, y1 = acc[nt][1] * gv.y;
                     const float y2 = acc[nt][2] * gv.x, y3 = acc[nt][3] * gv.y;
-                    SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA, c)) = pack_bf16(y0, y1);
-                    SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA + 8, c)) = pack_bf16(y2, y3);
+                    wy[nt][0] = pack_bf16(y0, y1);
+                    wy[nt][1] = pack_bf16(y2, y3);
                     bx[0][half] = pack_f16(acc[nt][0], acc[nt][1]);
                     bx[1][half] = pack_f16(acc[nt][2], acc[nt][3]);
                     by[0][half] = pack_f16(y0, y1);
                     by[1][half] = pack_f16(y2, y3);
                 }
-                const uint32_t koff = (2 * kk + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
-                if (n >= 1) {
-                    uint32_t aK[4];
-                    ldsm_x4_t(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
-                    mma_f16(cacc[0], aK, bx[0][0], bx[0][1]);
-                    mma_f16(cacc[1], aK, bx[1][0], bx[1][1]);
-                }
-                if (n >= 2) {
-                    uint32_t aK[4];
-                    ldsm_x4_t(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
-                    mma_f16(pacc[0], aK, by[0][0], by[0][1]);
-                    mma_f16(pacc[1], aK, by[1][0], by[1][1]);
-                }
+                mma_f16(cacc[0], aK1, bx[0][0], bx[0][1]);
+                mma_f16(cacc[1], aK1, bx[1][0], bx[1][1]);
+                mma_f16(pacc[0], aK2, by[0][0], by[0][1]);
+                mma_f16(pacc[1], aK2, by[1][0], by[1][1]);
             }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int c = 64 * chalf + 8 * nt + 2 * t;
+                SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA, c)) = wy[nt][0];
+                SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA + 8, c)) = wy[nt][1];
+            }
+            // sum the two channel halves (exchange through the dead hi tile), then
             // C^T / C'^T as [n = output column][k = j]
+            const uint32_t xc = scr + S_KLH + wrow * 2048 + lane * 16;
+            if (chalf) {
+                SM_AT(float4, xc) = make_float4(cacc[0][0], cacc[0][1], cacc[0][2], cacc[0][3]);
+                SM_AT(float4, xc + 512) = make_float4(cacc[1][0], cacc[1][1], cacc[1][2], cacc[1][3]);
+                SM_AT(float4, xc + 1024) = make_float4(pacc[0][0], pacc[0][1], pacc[0][2], pacc[0][3]);
+                SM_AT(float4, xc + 1536) = make_float4(pacc[1][0], pacc[1][1], pacc[1][2], pacc[1][3]);
+            }
+            named_bar_sync(bar_id, 128);
+            if (!chalf) {
+                const float4 x0 = SM_AT(const float4, xc), x1 = SM_AT(const float4, xc + 512);
+                const float4 x2 = SM_AT(const float4, xc + 1024), x3 = SM_AT(const float4, xc + 1536);
+                const float cs[2][4] = {{cacc[0][0] + x0.x, cacc[0][1] + x0.y, cacc[0][2] + x0.z, cacc[0][3] + x0.w},
+                                        {cacc[1][0] + x1.x, cacc[1][1] + x1.y, cacc[1][2] + x1.z, cacc[1][3] + x1.w}};
+                const float ps[2][4] = {{pacc[0][0] + x2.x, pacc[0][1] + x2.y, pacc[0][2] + x2.z, pacc[0][3] + x2.w},
+                                        {pacc[1][0] + x3.x, pacc[1][1] + x3.y, pacc[1][2] + x3.z, pacc[1][3] + x3.w}};
 #pragma unroll
-            for (int nu = 0; nu < 2; ++nu)
+                for (int nu = 0; nu < 2; ++nu)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int j = g + 8 * (i >> 1), col = 16 * lw + 8 * nu + 2 * t + (i & 1);
-                    if (n >= 1) SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cacc[nu][i]);
-                    if (n >= 2) SM_AT(uint16_t, sl + L_CP + cm16(col, j)) = f2h_bits(pacc[nu][i]);
-                }
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = g + 8 * (i >> 1), col = 16 * wrow + 8 * nu + 2 * t + (i & 1);
+                        // only chunks n >= 1 (C) and n >= 2 (C') are read by the tensor core
+                        SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cs[nu][i]);
+                        SM_AT(uint16_t, sl + L_CP + cm16(col, j)) = f2h_bits(ps[nu][i]);
+                    }
+            }
             tc::fence_async_smem();
-            const bool stop = named_bar_or(bar_id, 64, failed);
+            const bool stop = named_bar_or(bar_id, 128, failed);
             if (lt == 0) {
                 mbar_arrive(bar(B_PREP_FULL + n % NP));
                 if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));

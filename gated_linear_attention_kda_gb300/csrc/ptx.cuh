@@ -192,20 +192,20 @@ __device__ __forceinline__ void stsf2(uint32_t a, float x, float y)
     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
 }
 
+// ldmatrix is volatile (kept in order with the barrier and mbarrier asm, which
+// carry the memory clobbers) but does not fence ordinary shared-memory accesses.
 __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(a)
-                 : "memory");
+                 : "r"(a));
 }
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(a)
-                 : "memory");
+                 : "r"(a));
 }
 
 // ---------------------------------------------------------------- warp MMA
