@@ -49,9 +49,10 @@ struct Params {
 constexpr uint32_t WAIT_HINT_NS = 20000;
 constexpr int WAIT_LIMIT = 1 << 18;
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+// Slow path of wait_bar, kept out of line: the kernels wait at many sites and
+// inlined copies of the loop would crowd the instruction cache.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag)
 {
-    if (mbar_try_wait(bar, parity)) return true;
 #pragma unroll 1
     for (int i = 0; i < WAIT_LIMIT; ++i) {
         if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
@@ -62,8 +63,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return false;
 }
 
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag);
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight copies).
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
+__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity)
 {
 #pragma unroll 1
     for (int i = 0; i < WAIT_LIMIT; ++i)

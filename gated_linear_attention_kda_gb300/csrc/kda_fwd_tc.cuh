@@ -4,22 +4,25 @@
 //
 // Chunk algebra. For chunk n (16 tokens) with state S_n (V x K) at its start,
 // the prep lanes reduce the chunk to
-//   WX_n = [-w_n ; s q^_n] (32 x K),  TM_n = [T'_n ; s M_n] (32 x 16),
-//   Kbar_n (16 x K), gamma_n (K), V_n,
-// with T' = (I + A)^-1 diag(beta), w = T' (K*Gamma), M = P T',
-// q^ = Q*Gamma - M (K*Gamma), s = scale, so that one product gives both the
-// rows written into the state and the outputs:
-//   [E_n | O_n] = D_n = V_n^T TM_n^T + S_n WX_n^T,
+//   Z_n = [K*Gamma ; Q*Gamma] (32 x K),  Phi_n = [[-T', 0], [-s M, s I]] (32 x 32),
+//   TM_n = [T' ; s M] (32 x 16),  Kbar_n (16 x K),  gamma_n (K),  V_n,
+// with T' = (I + A)^-1 diag(beta), M = P T', s = scale, so that one product
+// gives both the rows written into the state and the outputs:
+//   [E_n | O_n] = D_n = V_n^T TM_n^T + S_n Z_n^T Phi_n^T,
 //   S_{n+1} = S_n Diag(gamma_n) + E_n Kbar_n.
-// The state product S_n WX_n^T streams the whole 128x128 state through the
-// tensor core; to keep it off the per-chunk dependency chain it is formed two
-// chunks ahead, from the decayed state two chunks back, and corrected by the
-// two rank-16 updates in between (exact in real arithmetic):
-//   S_n WX_n^T = bf16(S_{n-2} Gamma_{n-2}) WY_n^T + E_{n-2} C'_{n-2} + E_{n-1} C_{n-1},
-//   WY_n = WX_n Diag(gamma_{n-1}),  C_{n-1} = Kbar_{n-1} WX_n^T,
-//   C'_{n-2} = Kbar_{n-2} WY_n^T.
-// Only the last term depends on the previous chunk's result, so each chunk's
-// critical path is one 16-deep MMA plus one commit.
+// (Phi_n Z_n = [-w ; s q^] with w = T' (K*Gamma), q^ = Q*Gamma - M (K*Gamma).)
+// The state product is formed two chunks ahead from the decayed state two
+// chunks back and corrected by the two rank-16 updates in between (exact in
+// real arithmetic):
+//   S_n Z_n^T = Sb_{n-2} Z_n^T + E_{n-2} H''_n + E_{n-1} H_n,
+//   Sb_{n-2} = bf16(S_{n-2} Diag(gamma_{n-2} gamma_{n-1})),
+//   H_n = Kbar_{n-1} Z_n^T,  H''_n = Kbar_{n-2} Diag(gamma_{n-1}) Z_n^T,
+// so D_n = V_n^T TM_n^T + X_n Phi_n^T + E_{n-1} (H_n Phi_n^T), where
+// X_n = Sb_{n-2} Z_n^T + E_{n-2} H''_n is accumulated in tensor memory and
+// read back as the (tf32) A operand of the Phi product. Only the last term
+// depends on the previous chunk's result, so each chunk's critical path is one
+// 16-deep MMA plus one commit, and the prep lanes never form the 32 x K rows
+// of w and q^ themselves.
 //
 // Warp roles (448 threads):
 //   warp 0      TMA producer (lane 0); allocates / frees tensor memory.
@@ -29,7 +32,7 @@
 //               (S <- S Diag(gamma)) and keep its bf16 copy, store outputs.
 //   warps 6-13  two prep lanes of four warps, alternate chunks.
 // Tensor memory (512 columns): state fp32 [0,128), D x3 [128,224),
-// E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384).
+// E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384), X [384,416).
 //
 // Page references: base-2 gate with the LOG2E-folded scale and the tanh form
 // of the sigmoid ("FlashKDA lower_bound Parameter ..." -- "Conversion to the
@@ -45,7 +48,7 @@
 namespace kda {
 namespace tcs {
 
-constexpr int NR = 4;  // raw chunk ring
+constexpr int NR = 3;  // raw chunk ring
 constexpr int NP = 4;  // prep slot ring
 constexpr int NTHREADS = 448;
 
@@ -54,16 +57,18 @@ constexpr uint32_t T_S = 0;     // fp32 state, 128 columns
 constexpr uint32_t T_D = 128;   // D[3], 32 columns each
 constexpr uint32_t T_E = 224;   // E[2], 8 columns each (16 f16)
 constexpr uint32_t T_SB = 256;  // bf16 state copies [2], 64 columns each
+constexpr uint32_t T_X = 384;   // X, 32 fp32 columns
 
 // prep slot (bytes)
-constexpr int L_WY = 0;        // bf16, K-major 128B swizzle: 2 K-blocks x [32 rows][128 B]
+constexpr int L_Z = 0;         // bf16 Z, K-major 128B swizzle: 2 K-blocks x [32 rows][128 B]
 constexpr int L_V16 = 8192;    // f16 V, MN-major 128B swizzle: 2 boxes x [16 rows][128 B]
 constexpr int L_KB = 12288;    // f16 Kbar [128 n][16 k], K-major core matrices
-constexpr int L_TM = 16384;    // f16 [32 n][16 k]
-constexpr int L_CC = 17408;    // f16 C_{n-1}^T [32 n][16 k]
-constexpr int L_CP = 18432;    // f16 C'_{n-2}^T [32 n][16 k]
-constexpr int L_GAM = 19456;   // fp32 gamma [128]
-constexpr int SLOT = 20480;
+constexpr int L_PHI = 16384;   // fp32 Phi [32 n][32 k], K-major core matrices (LBO 128, SBO 1024)
+constexpr int L_TM = 20480;    // f16 TM [32 n][16 k]
+constexpr int L_CC = 21504;    // f16 (H Phi^T)^T [32 n][16 k]
+constexpr int L_HP = 22528;    // f16 H''^T [32 n][16 k]
+constexpr int L_GAM = 23552;   // fp32 gamma [128]
+constexpr int SLOT = 24576;
 
 // prep scratch (per lane); 16-bit tiles are [16][136] (272-byte rows)
 constexpr int H_LD = 272;
@@ -79,7 +84,7 @@ constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
 constexpr int S_TP = S_QG + 16 * H_LD;   // f16 T' [16][24]
 constexpr int S_PP = S_TP + 16 * M_LD;   // f16 P [16][24]
 constexpr int S_BETA = S_PP + 16 * M_LD; // fp32 beta [16]
-constexpr int S_GX = S_BETA + 64;        // fp32x2 [2 halves][64 pairs]: gate sums exchanged between row halves
+constexpr int S_GX = S_BETA + 64;        // fp32 [2][64][2]: gate sums between row halves; later s H^q fragments
 constexpr int S_AX = S_GX + 1024;        // fp32 [2][2][32 lanes][4]: second channel half of A and P
 constexpr int SCR = S_AX + 2048;
 
@@ -95,7 +100,8 @@ constexpr int OFF_FLAGS = OFF_TMEMPTR + 16;
 constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 
-static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(NR <= 4 && NP <= 4, "barrier index ranges");
+static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && S_AX % 16 == 0 && SCR % 16 == 0, "alignment");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -106,11 +112,44 @@ __device__ __forceinline__ uint32_t cm16(int n, int k)
 {
     return (n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
 }
+// byte offset of (row n, col k) in a K-major, non-swizzled fp32 (tf32) operand
+// with 32 K elements per row: 8 x 4 core matrices, LBO = 128 (K), SBO = 1024 (N)
+__device__ __forceinline__ uint32_t cm32(int n, int k)
+{
+    return (n >> 3) * 1024 + (k >> 2) * 128 + (n & 7) * 16 + (k & 3) * 4;
+}
 // byte offset of (row, col) in a bf16 K-major 128B-swizzled operand, K = 128
 // as two 64-column blocks of 32 rows
 __device__ __forceinline__ uint32_t sw128_32rows(int row, int c)
 {
     return (c >> 6) * 4096 + row * 128 + ((((c & 63) >> 3) ^ (row & 7)) << 4) + (c & 7) * 2;
+}
+__device__ __forceinline__ float h_lo(uint32_t w) { return __low2float(*reinterpret_cast<const __half2 *>(&w)); }
+__device__ __forceinline__ float h_hi(uint32_t w) { return __high2float(*reinterpret_cast<const __half2 *>(&w)); }
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// D_n = V_n^T TM_n^T + (Sb[b] Z_n^T [+ E[e] H''_n]) Phi_n^T for the prep slot at `sl`
+// (one issuing thread; kept out of line, it is issued from two sites).
+__device__ __noinline__ void issue_d(uint32_t tmem, uint32_t sl, int dbuf, int b, int e)
+{
+    const uint32_t id_u = tc::idesc(tc::F16, 128, 32, 1, 0);
+    const uint32_t id_c = tc::idesc(tc::F16, 128, 32, 0, 0);
+    const uint32_t id_y = tc::idesc(tc::BF16, 128, 32, 0, 0);
+    const uint32_t id_p = tc::idesc(tc::TF32, 128, 32, 0, 0);
+    const uint32_t dn = tmem + T_D + 32 * dbuf, x = tmem + T_X;
+    tc::mma_ss(dn, tc::sdesc(sl + L_V16, 2048, 1024, tc::SWZ_128B), tc::sdesc(sl + L_TM, 128, 256, tc::SWZ_NONE), id_u, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        tc::mma_ts(x, tmem + T_SB + 64 * b + 8 * i, tc::sdesc(sl + L_Z + (i >> 2) * 4096 + (i & 3) * 32, 16, 1024, tc::SWZ_128B),
+                   id_y, i > 0);
+    if (e >= 0) tc::mma_ts(x, tmem + T_E + 8 * e, tc::sdesc(sl + L_HP, 128, 256, tc::SWZ_NONE), id_c, 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        tc::mma_ts_tf32(dn, x + 8 * i, tc::sdesc(sl + L_PHI + 256 * i, 128, 1024, tc::SWZ_NONE), id_p, 1);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -195,31 +234,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0 && nch > 0) {
-            const uint32_t id_u = tc::idesc(tc::F16, 128, 32, 1, 0);
             const uint32_t id_c = tc::idesc(tc::F16, 128, 32, 0, 0);
-            const uint32_t id_y = tc::idesc(tc::BF16, 128, 32, 0, 0);
             const uint32_t id_s = tc::idesc(tc::F16, 128, 128, 0, 0);
-            // D_n = V_n^T TM_n^T (fresh)
-            auto issue_u = [&](int n) {
-                const uint32_t sl = slot(n);
-                tc::mma_ss(tmem + T_D + 32 * (n % 3), tc::sdesc(sl + L_V16, 2048, 1024, tc::SWZ_128B),
-                           tc::sdesc(sl + L_TM, 128, 256, tc::SWZ_NONE), id_u, 0);
-            };
-            // D_n += Sb[b] WY_n^T
-            auto issue_y = [&](int n, int b) {
-                const uint32_t sl = slot(n);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    tc::mma_ts(tmem + T_D + 32 * (n % 3), tmem + T_SB + 64 * b + 8 * i,
-                               tc::sdesc(sl + L_WY + (i >> 2) * 4096 + (i & 3) * 32, 16, 1024, tc::SWZ_128B), id_y, 1);
-            };
             bool ok = wait_bar(bar(B_I), 0, flags);
             for (int n = 0; ok && n < (nch < 2 ? nch : 2); ++n) {
                 ok = wait_bar(bar(B_PREP_FULL + n % NP), (n / NP) & 1, flags);
                 if (!ok) break;
                 tc::fence_after();
-                issue_u(n);
-                issue_y(n, n & 1);
+                issue_d(tmem, slot(n), n % 3, n & 1, -1);
                 if (n == 0) tc::commit(bar(B_D + 0));
             }
             for (int k = 0; ok && k < nch; ++k) {
@@ -227,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!ok) break;
                 tc::fence_after();
                 const uint32_t e = tmem + T_E + 8 * (k & 1);
-                if (k + 1 < nch) {  // D_{k+1} += E_k C_k
+                if (k + 1 < nch) {  // D_{k+1} += E_k (H_{k+1} Phi_{k+1}^T)
                     tc::mma_ts(tmem + T_D + 32 * ((k + 1) % 3), e, tc::sdesc(slot(k + 1) + L_CC, 128, 256, tc::SWZ_NONE),
                                id_c, 1);
                     tc::commit(bar(B_D + ((k + 1) & 1)));
@@ -239,14 +261,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc::mma_ts(tmem + T_S, e, tc::sdesc(slot(k) + L_KB, 128, 256, tc::SWZ_NONE), id_s, 1);
                 tc::commit(bar(B_S + (k & 1)));
                 tc::commit(bar(B_PREP_EMPTY + k % NP));
-                if (k + 2 < nch) {  // D_{k+2} = U + E_k C'_k + Sb[k] WY^T
+                if (k + 2 < nch) {
                     const int n = k + 2;
                     ok = wait_bar(bar(B_PREP_FULL + n % NP), (n / NP) & 1, flags);
                     if (!ok) break;
                     tc::fence_after();
-                    issue_u(n);
-                    tc::mma_ts(tmem + T_D + 32 * (n % 3), e, tc::sdesc(slot(n) + L_CP, 128, 256, tc::SWZ_NONE), id_c, 1);
-                    issue_y(n, k & 1);
+                    issue_d(tmem, slot(n), n % 3, k & 1, k & 1);
                 }
             }
             tc::commit(bar(B_F));
@@ -258,38 +278,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = 32 * q4 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const size_t st_row = (static_cast<size_t>(seq) * p.H + h) * (DH * DH) + static_cast<size_t>(row) * DH;
+        // S_0, bf16(S_0) for chunk 0's product and bf16(S_0 Diag(gamma_0)) for chunk 1's
+        bool ok = nch == 0 || wait_bar(bar(B_PREP_FULL + 0), 0, flags);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after();
 #pragma unroll 1
         for (int g4 = 0; g4 < 4; ++g4) {
-            uint32_t r32[32], r16[16];
+            uint32_t r32[32], r16[16], r16g[16];
+            if (!p.init) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r32[i] = 0u;
+            } else if (p.init_dtype == KDA_DTYPE_FP32) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const float *>(p.init) + st_row + 32 * g4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 w = src[i];
+                    r32[4 * i] = w.x;
+                    r32[4 * i + 1] = w.y;
+                    r32[4 * i + 2] = w.z;
+                    r32[4 * i + 3] = w.w;
+                }
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.init) + st_row + 32 * g4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 w = src[i];
+                    r32[8 * i] = w.x << 16;
+                    r32[8 * i + 1] = w.x & 0xffff0000u;
+                    r32[8 * i + 2] = w.y << 16;
+                    r32[8 * i + 3] = w.y & 0xffff0000u;
+                    r32[8 * i + 4] = w.z << 16;
+                    r32[8 * i + 5] = w.z & 0xffff0000u;
+                    r32[8 * i + 6] = w.w << 16;
+                    r32[8 * i + 7] = w.w & 0xffff0000u;
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.init) {
-                    if (p.init_dtype == KDA_DTYPE_FP32) {
-                        v = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + st_row + 32 * g4 + i);
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.init) + st_row + 32 * g4 + i);
-                        v = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-                    }
-                }
-                r32[i] = __float_as_uint(v.x);
-                r32[i + 1] = __float_as_uint(v.y);
-                r32[i + 2] = __float_as_uint(v.z);
-                r32[i + 3] = __float_as_uint(v.w);
-                r16[i / 2] = pack_bf16(v.x, v.y);
-                r16[i / 2 + 1] = pack_bf16(v.z, v.w);
+                const float4 g0 = nch > 0 ? SM_AT(const float4, slot(0) + L_GAM + (32 * g4 + i) * 4) : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float x0 = __uint_as_float(r32[i]), x1 = __uint_as_float(r32[i + 1]);
+                const float x2 = __uint_as_float(r32[i + 2]), x3 = __uint_as_float(r32[i + 3]);
+                r16[i / 2] = pack_bf16(x0, x1);
+                r16[i / 2 + 1] = pack_bf16(x2, x3);
+                r16g[i / 2] = pack_bf16(x0 * g0.x, x1 * g0.y);
+                r16g[i / 2 + 1] = pack_bf16(x2 * g0.z, x3 * g0.w);
             }
             tc::st32(lb + T_S + 32 * g4, r32);
             tc::st16(lb + T_SB + 16 * g4, r16);
-            tc::st16(lb + T_SB + 64 + 16 * g4, r16);
+            tc::st16(lb + T_SB + 64 + 16 * g4, r16g);
         }
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_I));
 
-        bool ok = true;
-        for (int k = 0; k < nch; ++k) {
+        for (int k = 0; ok && k < nch; ++k) {
             ok = wait_bar(bar(B_D + (k & 1)), (k >> 1) & 1, flags);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
@@ -309,59 +352,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_E + (k & 1)));
             }
-            // decay the state for this chunk: S <- S Diag(gamma_k), and its bf16 copy
+            // decay the state for this chunk, S <- S Diag(gamma_k), and keep
+            // bf16(S Diag(gamma_k gamma_{k+1})) for chunk k + 2's product
+            const bool more = k + 1 < nch;
             ok = (k == 0) || wait_bar(bar(B_S + ((k - 1) & 1)), ((k - 1) >> 1) & 1, flags);
             ok = ok && wait_bar(bar(B_PREP_FULL + k % NP), (k / NP) & 1, flags);
+            ok = ok && (!more || wait_bar(bar(B_PREP_FULL + (k + 1) % NP), ((k + 1) / NP) & 1, flags));
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after();
-            const uint32_t gam = slot(k) + L_GAM;
-            // four 32-column blocks, the next block's load in flight while one is decayed
+            const uint32_t gam = slot(k) + L_GAM, gnx = slot(k + 1) + L_GAM;
             auto decay_block = [&](int g4, uint32_t(&r32)[32]) {
                 uint32_t r16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
+                    const float4 gl = SM_AT(const float4, gnx + (32 * g4 + i) * 4);
+                    const float4 gn = more ? gl : make_float4(1.f, 1.f, 1.f, 1.f);
                     const float a0 = __uint_as_float(r32[i]) * gv.x, a1 = __uint_as_float(r32[i + 1]) * gv.y;
                     const float a2 = __uint_as_float(r32[i + 2]) * gv.z, a3 = __uint_as_float(r32[i + 3]) * gv.w;
                     r32[i] = __float_as_uint(a0);
                     r32[i + 1] = __float_as_uint(a1);
                     r32[i + 2] = __float_as_uint(a2);
                     r32[i + 3] = __float_as_uint(a3);
-                    r16[i / 2] = pack_bf16(a0, a1);
-                    r16[i / 2 + 1] = pack_bf16(a2, a3);
+                    r16[i / 2] = pack_bf16(a0 * gn.x, a1 * gn.y);
+                    r16[i / 2 + 1] = pack_bf16(a2 * gn.z, a3 * gn.w);
                 }
                 tc::st32(lb + T_S + 32 * g4, r32);
                 tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);
             };
-            {
-                uint32_t ra[32], rb[32];
-                tc::ld32(lb + T_S, ra);
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint32_t ra[32];
+                tc::ld32(lb + T_S + 32 * g4, ra);
                 tc::wait_ld();
-                tc::ld32(lb + T_S + 32, rb);
-                decay_block(0, ra);
-                tc::wait_ld();
-                tc::ld32(lb + T_S + 64, ra);
-                decay_block(1, rb);
-                tc::wait_ld();
-                tc::ld32(lb + T_S + 96, rb);
-                decay_block(2, ra);
-                tc::wait_ld();
-                decay_block(3, rb);
+                decay_block(g4, ra);
             }
             tc::wait_st();
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_G + (k & 1)));
-            // outputs (already scaled)
-            const int tok0 = sp.bos + k * CHUNK;
+            // outputs (already scaled): one bf16 per token row, stepping by the token stride
             const int Lv = min(CHUNK, sp.len - k * CHUNK);
+            uint16_t *op = p.out + (static_cast<size_t>(sp.bos + k * CHUNK) * p.H + h) * DH + row;
+            const size_t ostride = static_cast<size_t>(p.H) * DH;
 #pragma unroll
-            for (int r = 0; r < CHUNK; ++r)
-                if (r < Lv)
-                    p.out[(static_cast<size_t>(tok0 + r) * p.H + h) * DH + row] = f2bf_bits(__uint_as_float(d[16 + r]));
+            for (int r = 0; r < CHUNK; ++r) {
+                if (r < Lv) *op = f2bf_bits(__uint_as_float(d[16 + r]));
+                op += ostride;
+            }
         }
         if (p.fin) {
             if (ok && nch > 0) ok = wait_bar(bar(B_S + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1, flags);
@@ -393,8 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // ---------------------------------------------------------------- prep lanes
         // lane = 4 warps = 128 threads. Element-wise passes: thread -> channel pair
-        // (c0, c0 + 1), rows [8 rh, 8 rh + 8). Products: warp lw, row block
-        // wrow = lw >> 1 of WX (0: -w, 1: s q^), channel half chalf = lw & 1.
+        // (c0, c0 + 1), rows [8 rh, 8 rh + 8).
         const int ln = (warp - 6) >> 2;
         const int lt = threadIdx.x - 192 - 128 * ln;  // 0..127
         const int lw = lt >> 5;
@@ -402,7 +442,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
         const int cp = lt & 63, rh = lt >> 6;
         const int c0 = 2 * cp, r0 = 8 * rh;
-        const int wrow = lw >> 1, chalf = lw & 1;
         // x / 2 = ah2 * g + bb, with x = exp(A_log) (g + dt_bias)
         float ah2 = 0.5f, bb0 = 0.f, bb1 = 0.f;
         if (p.A_log) ah2 = 0.5f * ex2_approx(__ldg(p.A_log + h) * LOG2E);
@@ -413,6 +452,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float hs = p.half_gs, sc = p.scale;
         const int g = lane >> 2, t = lane & 3;
         const int mi = lane >> 3, ri = lane & 7;
+        // B operand (n = tile row, k = tile column) of a row-major [16][136] 16-bit tile
+        const uint32_t b_row = (ri + 8 * (mi >> 1)) * H_LD + 16 * (mi & 1);
 
         for (int n = ln; n < nch; n += 2) {
             bool failed = false;
@@ -479,9 +520,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float k0 = bf16_lo(kw), k1 = bf16_hi(kw), q0 = bf16_lo(qw), q1 = bf16_hi(qw);
                 const float kl0 = k0 * u0, kl1 = k1 * u1, ql0 = q0 * u0, ql1 = q1 * u1;
                 const float kr0 = k0 * f0, kr1 = k1 * f1;
+                const float kg0 = kl0 * gr0, kg1 = kl1 * gr1, qg0 = ql0 * gr0, qg1 = ql1 * gr1;  // K, Q * Gamma
                 const uint32_t o = r * H_LD + c0 * 2;
-                SM_AT(uint32_t, scr + S_KG + o) = pack_f16(kl0 * gr0, kl1 * gr1);  // K * Gamma
-                SM_AT(uint32_t, scr + S_QG + o) = pack_f16(ql0 * gr0, ql1 * gr1);  // Q * Gamma
+                SM_AT(uint32_t, scr + S_KG + o) = pack_f16(kg0, kg1);
+                SM_AT(uint32_t, scr + S_QG + o) = pack_f16(qg0, qg1);
+                SM_AT(uint32_t, sl + L_Z + sw128_32rows(r, c0)) = pack_bf16(kg0, kg1);
+                SM_AT(uint32_t, sl + L_Z + sw128_32rows(16 + r, c0)) = pack_bf16(qg0, qg1);
                 SM_AT(uint32_t, sl + L_V16 + raw_off(r, c0)) = pack_f16(bf16_lo(vw), bf16_hi(vw));
                 uint32_t hi, lo;
                 split_bf16_trunc(kl0, kl1, hi, lo);
@@ -506,12 +550,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
             // A (warps 0, 2) and P (warps 1, 3), each warp over one channel half;
             // three bf16 products per entry (hi/lo split)
+            const bool isP = lw & 1;
+            const int khalf = lw >> 1;
+            Frag16 acc;
+            chunk_gram_x3<4>(scr + (isP ? S_QLH : S_KLH), scr + (isP ? S_QLL : S_KLL), scr + S_KRH, scr + S_KRL, acc, lane,
+                             4 * khalf);
             {
-                const bool isP = lw & 1;
-                const int khalf = lw >> 1;
-                Frag16 acc;
-                chunk_gram_x3<4>(scr + (isP ? S_QLH : S_KLH), scr + (isP ? S_QLL : S_KLL), scr + S_KRH, scr + S_KRL, acc,
-                                 lane, 4 * khalf);
                 const uint32_t xa = scr + S_AX + (isP ? 1024 : 0) + lane * 16;
                 if (khalf) {
                     SM_AT(float4, xa) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
@@ -522,183 +566,160 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float4 x0 = SM_AT(const float4, xa), x1 = SM_AT(const float4, xa + 512);
                     acc.c[0][0] += x0.x; acc.c[0][1] += x0.y; acc.c[0][2] += x0.z; acc.c[0][3] += x0.w;
                     acc.c[1][0] += x1.x; acc.c[1][1] += x1.y; acc.c[1][2] += x1.z; acc.c[1][3] += x1.w;
-                    if (!isP) {
-                        // A = strictly-lower, rows scaled by beta; T' = (I + A)^-1 diag(beta)
-                        const float bg = SM_AT(const float, scr + S_BETA + g * 4);
-                        const float bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
-                                acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
-                            }
-                        Frag16 T;
-                        unit_lower_inverse(acc, T, g, t);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const int col = 8 * nt + 2 * t;
-                            const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int r = g + 8 * hh;
-                                const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
-                                SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
-                                SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
-                            }
-                        }
-                    } else {
-                        // P = lower (diagonal included)
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int r = g + 8 * hh, j = 8 * nt + 2 * t;
-                                const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
-                                const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
-                                SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
-                            }
-                    }
-                }
-                named_bar_sync(bar_id, 128);
-            }
-
-            // WX rows 16 wrow.. (0: -w = -T' (K*Gamma); 1: s q^ = s (Q*Gamma) - s M (K*Gamma)),
-            // channels 64 chalf..
-            float acc[8][4];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-            {
-                uint32_t aX[4];
-                if (wrow == 0) {
-                    ldsm_x4(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aX[0], aX[1], aX[2], aX[3]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) aX[i] ^= 0x80008000u;
-                } else {
-                    // M = P T' (16 x 16 x 16); TM rows 16..31 = s M
-                    uint32_t aP[4], b0, b1, b2, b3;
-                    ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
-                    ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
-                    float m[2][4];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) m[i][0] = m[i][1] = m[i][2] = m[i][3] = 0.f;
-                    mma_f16(m[0], aP, b0, b1);
-                    mma_f16(m[1], aP, b2, b3);
-                    if (chalf == 0) {
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int r = g + 8 * hh, col = 8 * nt + 2 * t;
-                                SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) =
-                                    pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
-                            }
-                    }
-                    aX[0] = pack_f16(-sc * m[0][0], -sc * m[0][1]);
-                    aX[1] = pack_f16(-sc * m[0][2], -sc * m[0][3]);
-                    aX[2] = pack_f16(-sc * m[1][0], -sc * m[1][1]);
-                    aX[3] = pack_f16(-sc * m[1][2], -sc * m[1][3]);
-                }
-                const uint32_t bkg = scr + S_KG + (ri + 8 * (mi & 1)) * H_LD + 128 * chalf + 16 * (mi >> 1);
-#pragma unroll
-                for (int m8 = 0; m8 < 4; ++m8) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(bkg + 32 * m8, b0, b1, b2, b3);
-                    mma_f16(acc[2 * m8], aX, b0, b1);
-                    mma_f16(acc[2 * m8 + 1], aX, b2, b3);
-                }
-                if (wrow == 1) {
-                    // + s * I * (Q*Gamma)
-                    const uint32_t sh = static_cast<uint32_t>(f2h_bits(sc));
-                    uint32_t aI[4];
-                    aI[0] = (g == 2 * t ? sh : 0u) | (g == 2 * t + 1 ? sh << 16 : 0u);
-                    aI[1] = 0u;
-                    aI[2] = 0u;
-                    aI[3] = aI[0];
-                    const uint32_t bqg = scr + S_QG + (ri + 8 * (mi & 1)) * H_LD + 128 * chalf + 16 * (mi >> 1);
-#pragma unroll
-                    for (int m8 = 0; m8 < 4; ++m8) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(bqg + 32 * m8, b0, b1, b2, b3);
-                        mma_f16(acc[2 * m8], aI, b0, b1);
-                        mma_f16(acc[2 * m8 + 1], aI, b2, b3);
-                    }
                 }
             }
-
-            // cross-chunk terms: gamma_{n-1}, Kbar_{n-1}, Kbar_{n-2}; partial sums over
-            // this warp's channel half
-            if (n >= 1 && !wait_bar(bar(B_PREP_FULL + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+            // cross-chunk products on warps 1..3 while warp 0 inverts (slots n-1, n-2)
             const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
-            const int rowA = 16 * wrow + g;
-            float cacc[2][4], pacc[2][4];
+            Frag16 hw;  // warp 1: H^w = Kbar_{n-1} (K*Gamma)^T;  warp 2: H^q = Kbar_{n-1} (Q*Gamma)^T
+            frag_zero(hw);
+            if (lw == 0) {
+                // A = strictly-lower, rows scaled by beta; T' = (I + A)^-1 diag(beta)
+                const float bg = SM_AT(const float, scr + S_BETA + g * 4);
+                const float bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                cacc[i][0] = cacc[i][1] = cacc[i][2] = cacc[i][3] = 0.f;
-                pacc[i][0] = pacc[i][1] = pacc[i][2] = pacc[i][3] = 0.f;
-            }
-            uint32_t wy[8][2];  // bf16 WY pairs, stored after the products
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                // WX / WY columns c in [64 chalf + 16 kk, +16)
-                const int kb = 4 * chalf + kk;
-                const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
-                // branch-free: for n < 2 the products read stale slots and are never stored / used
-                uint32_t aK1[4], aK2[4];
-                ldsm_x4_t(prev + L_KB + koff, aK1[0], aK1[1], aK1[2], aK1[3]);
-                ldsm_x4_t(prev2 + L_KB + koff, aK2[0], aK2[1], aK2[2], aK2[3]);
-                uint32_t bx[2][2], by[2][2];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int nt = 2 * kk + half, c = 16 * kb + 8 * half + 2 * t;
-                    const float2 gl = SM_AT(const float2, prev + L_GAM + c * 4);
-                    const float2 gv = n >= 1 ? gl : make_float2(1.f, 1.f);
-                    const float y0 = acc[nt][0] * gv.x, y1 = acc[nt][1] * gv.y;
-                    const float y2 = acc[nt][2] * gv.x, y3 = acc[nt][3] * gv.y;
-                    wy[nt][0] = pack_bf16(y0, y1);
-                    wy[nt][1] = pack_bf16(y2, y3);
-                    bx[0][half] = pack_f16(acc[nt][0], acc[nt][1]);
-                    bx[1][half] = pack_f16(acc[nt][2], acc[nt][3]);
-                    by[0][half] = pack_f16(y0, y1);
-                    by[1][half] = pack_f16(y2, y3);
-                }
-                mma_f16(cacc[0], aK1, bx[0][0], bx[0][1]);
-                mma_f16(cacc[1], aK1, bx[1][0], bx[1][1]);
-                mma_f16(pacc[0], aK2, by[0][0], by[0][1]);
-                mma_f16(pacc[1], aK2, by[1][0], by[1][1]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int c = 64 * chalf + 8 * nt + 2 * t;
-                SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA, c)) = wy[nt][0];
-                SM_AT(uint32_t, sl + L_WY + sw128_32rows(rowA + 8, c)) = wy[nt][1];
-            }
-            // sum the two channel halves (exchange through the dead hi tile), then
-            // C^T / C'^T as [n = output column][k = j]
-            const uint32_t xc = scr + S_KLH + wrow * 2048 + lane * 16;
-            if (chalf) {
-                SM_AT(float4, xc) = make_float4(cacc[0][0], cacc[0][1], cacc[0][2], cacc[0][3]);
-                SM_AT(float4, xc + 512) = make_float4(cacc[1][0], cacc[1][1], cacc[1][2], cacc[1][3]);
-                SM_AT(float4, xc + 1024) = make_float4(pacc[0][0], pacc[0][1], pacc[0][2], pacc[0][3]);
-                SM_AT(float4, xc + 1536) = make_float4(pacc[1][0], pacc[1][1], pacc[1][2], pacc[1][3]);
-            }
-            named_bar_sync(bar_id, 128);
-            if (!chalf) {
-                const float4 x0 = SM_AT(const float4, xc), x1 = SM_AT(const float4, xc + 512);
-                const float4 x2 = SM_AT(const float4, xc + 1024), x3 = SM_AT(const float4, xc + 1536);
-                const float cs[2][4] = {{cacc[0][0] + x0.x, cacc[0][1] + x0.y, cacc[0][2] + x0.z, cacc[0][3] + x0.w},
-                                        {cacc[1][0] + x1.x, cacc[1][1] + x1.y, cacc[1][2] + x1.z, cacc[1][3] + x1.w}};
-                const float ps[2][4] = {{pacc[0][0] + x2.x, pacc[0][1] + x2.y, pacc[0][2] + x2.z, pacc[0][3] + x2.w},
-                                        {pacc[1][0] + x3.x, pacc[1][1] + x3.y, pacc[1][2] + x3.z, pacc[1][3] + x3.w}};
-#pragma unroll
-                for (int nu = 0; nu < 2; ++nu)
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int j = g + 8 * (i >> 1), col = 16 * wrow + 8 * nu + 2 * t + (i & 1);
-                        // only chunks n >= 1 (C) and n >= 2 (C') are read by the tensor core
-                        SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cs[nu][i]);
-                        SM_AT(uint16_t, sl + L_CP + cm16(col, j)) = f2h_bits(ps[nu][i]);
+                        const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
+                        acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
                     }
+                Frag16 T;
+                unit_lower_inverse(acc, T, g, t);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 8 * nt + 2 * t;
+                    const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = g + 8 * hh;
+                        const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
+                        SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
+                        SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
+                        // Phi rows 0..15: [-T', 0]
+                        SM_AT(float2, sl + L_PHI + cm32(r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                        SM_AT(float2, sl + L_PHI + cm32(r, 16 + col)) = make_float2(0.f, 0.f);
+                    }
+                }
+            } else {
+                if (lw == 1) {
+                    // P = lower (diagonal included)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh, j = 8 * nt + 2 * t;
+                            const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
+                            const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
+                            SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
+                        }
+                }
+                if (n >= 1 && !wait_bar(bar(B_PREP_FULL + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+                // for n < 2 the products below read stale slots; they are stored but never used
+                if (lw < 3) {
+                    const uint32_t zt = scr + (lw == 1 ? S_KG : S_QG) + b_row;
+#pragma unroll
+                    for (int kb = 0; kb < 8; ++kb) {
+                        const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                        uint32_t aK[4], bz[4];
+                        ldsm_x4_t(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
+                        mma_f16(hw.c[0], aK, bz[0], bz[1]);
+                        mma_f16(hw.c[1], aK, bz[2], bz[3]);
+                    }
+                    if (lw == 2) {  // s H^q for warp 1
+                        const uint32_t xh = scr + S_GX + lane * 16;
+                        SM_AT(float4, xh) = make_float4(sc * hw.c[0][0], sc * hw.c[0][1], sc * hw.c[0][2], sc * hw.c[0][3]);
+                        SM_AT(float4, xh + 512) = make_float4(sc * hw.c[1][0], sc * hw.c[1][1], sc * hw.c[1][2], sc * hw.c[1][3]);
+                    }
+                } else {
+                    // H'' = Kbar_{n-2} Diag(gamma_{n-1}) Z^T (16 x 32), stored as [n = column][k = j]
+                    float hp[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) hp[i][0] = hp[i][1] = hp[i][2] = hp[i][3] = 0.f;
+#pragma unroll
+                    for (int kb = 0; kb < 8; ++kb) {
+                        const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                        uint32_t aK[4], bk[4], bq[4];
+                        ldsm_x4_t(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(scr + S_KG + b_row + 32 * kb, bk[0], bk[1], bk[2], bk[3]);
+                        ldsm_x4(scr + S_QG + b_row + 32 * kb, bq[0], bq[1], bq[2], bq[3]);
+                        const float2 gl = SM_AT(const float2, prev + L_GAM + (16 * kb + 2 * t) * 4);
+                        const float2 gh = SM_AT(const float2, prev + L_GAM + (16 * kb + 8 + 2 * t) * 4);
+                        const uint32_t gk0 = pack_f16(gl.x, gl.y), gk1 = pack_f16(gh.x, gh.y);
+                        mma_f16(hp[0], aK, hmul2(bk[0], gk0), hmul2(bk[1], gk1));
+                        mma_f16(hp[1], aK, hmul2(bk[2], gk0), hmul2(bk[3], gk1));
+                        mma_f16(hp[2], aK, hmul2(bq[0], gk0), hmul2(bq[1], gk1));
+                        mma_f16(hp[3], aK, hmul2(bq[2], gk0), hmul2(bq[3], gk1));
+                    }
+#pragma unroll
+                    for (int nu = 0; nu < 4; ++nu)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = g + 8 * (i >> 1), col = 8 * nu + 2 * t + (i & 1);
+                            SM_AT(uint16_t, sl + L_HP + cm16(col, j)) = f2h_bits(hp[nu][i]);
+                        }
+                }
+            }
+            named_bar_sync(bar_id, 128);
+
+            // M = P T' (warps 0, 1): warp 0 writes TM rows 16..31 = s M and Phi rows 16..31 =
+            // [-s M, s I]; warp 1 writes (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q]
+            if (lw < 2) {
+                uint32_t aP[4], b0, b1, b2, b3;
+                ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
+                ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
+                float m[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) m[i][0] = m[i][1] = m[i][2] = m[i][3] = 0.f;
+                mma_f16(m[0], aP, b0, b1);
+                mma_f16(m[1], aP, b2, b3);
+                // s M rounded to f16 once, shared by TM, Phi and the correction
+                uint32_t sm16[2][2];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) sm16[nt][hh] = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
+                if (lw == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = g + 8 * hh, col = 8 * nt + 2 * t;
+                            const uint32_t w = sm16[nt][hh];
+                            SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = w;
+                            SM_AT(float2, sl + L_PHI + cm32(16 + r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                            SM_AT(float2, sl + L_PHI + cm32(16 + r, 16 + col)) =
+                                make_float2(r == col ? sc : 0.f, r == col + 1 ? sc : 0.f);
+                        }
+                } else {
+                    // A operand: H^w (rows j, k = m)
+                    uint32_t aH[4];
+                    frag_as_a(hw, aH);
+                    float cf[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
+                    // B[k = m][n] = -T'[n][m]: the T' tile rows are n
+                    uint32_t bt[4];
+                    ldsm_x4(scr + S_TP + (ri + 8 * (mi >> 1)) * M_LD + 16 * (mi & 1), bt[0], bt[1], bt[2], bt[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) bt[i] ^= 0x80008000u;
+                    mma_f16(cf[0], aH, bt[0], bt[1]);
+                    mma_f16(cf[1], aH, bt[2], bt[3]);
+                    // B[k = m][n = i] = -s M[i][m], from the accumulator fragments of M
+                    mma_f16(cf[2], aH, sm16[0][0] ^ 0x80008000u, sm16[1][0] ^ 0x80008000u);
+                    mma_f16(cf[3], aH, sm16[0][1] ^ 0x80008000u, sm16[1][1] ^ 0x80008000u);
+                    const uint32_t xh = scr + S_GX + lane * 16;
+                    const float4 q0 = SM_AT(const float4, xh), q1 = SM_AT(const float4, xh + 512);
+                    cf[2][0] += q0.x; cf[2][1] += q0.y; cf[2][2] += q0.z; cf[2][3] += q0.w;
+                    cf[3][0] += q1.x; cf[3][1] += q1.y; cf[3][2] += q1.z; cf[3][3] += q1.w;
+#pragma unroll
+                    for (int nu = 0; nu < 4; ++nu)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = g + 8 * (i >> 1), col = 8 * nu + 2 * t + (i & 1);
+                            SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cf[nu][i]);
+                        }
+                }
             }
             tc::fence_async_smem();
             const bool stop = named_bar_or(bar_id, 128, failed);

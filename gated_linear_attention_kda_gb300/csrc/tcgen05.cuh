@@ -81,6 +81,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::tf32 (A holds fp32 words)
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+                 : "memory");
+}
+
 // 32 lanes (this warp's quarter) x 32 consecutive 32-bit columns
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
 {
