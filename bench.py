@@ -36,7 +36,7 @@ FLOPS_PER_CHUNK_HEAD = 3 * 2 * 16 * 128 * 128 + 5 * 2 * 16 * 16 * 128 + 2 * 16 *
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 KERNEL_SOURCES = ["gated_linear_attention_kda_gb300/csrc/" + f for f in
                   ("kda_fwd.cu", "ptx.cuh", "kda_common.cuh", "kda_chunk.cuh", "kda_fwd_mma.cuh", "tcgen05.cuh", "kda_fwd_tc.cuh")]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_kernel.b8_t4096_h16.traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_tc_kernel.b8_t4096_h16.traffic.json")
 
 
 def kernel_hash() -> str:
