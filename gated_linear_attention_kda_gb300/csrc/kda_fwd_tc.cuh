@@ -95,7 +95,8 @@ constexpr int OFF_BAR = OFF_SCR + 2 * SCR;
 // barrier indices
 constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_PREP_FULL = 8, B_PREP_EMPTY = 12, B_D = 16, B_E = 18, B_G = 20,
               B_S = 22, B_I = 24, B_F = 25, NBARS = 26;
-constexpr int OFF_TMEMPTR = OFF_BAR + NBARS * 8;
+constexpr int OFF_ONES = OFF_BAR + NBARS * 8;  // fp32 [128] of 1.0: gamma after the last chunk
+constexpr int OFF_TMEMPTR = OFF_ONES + DH * 4;
 constexpr int OFF_FLAGS = OFF_TMEMPTR + 16;
 constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         flags[0] = 0;
         fence_mbar_init();
     }
+    if (threadIdx.x < DH) SM_AT(float, sb + OFF_ONES + threadIdx.x * 4) = 1.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -363,22 +365,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc::fence_after();
-            const uint32_t gam = slot(k) + L_GAM, gnx = slot(k + 1) + L_GAM;
+            const uint32_t gam = slot(k) + L_GAM, gnx = more ? slot(k + 1) + L_GAM : sb + OFF_ONES;
             auto decay_block = [&](int g4, uint32_t(&r32)[32]) {
                 uint32_t r16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
-                    const float4 gl = SM_AT(const float4, gnx + (32 * g4 + i) * 4);
-                    const float4 gn = more ? gl : make_float4(1.f, 1.f, 1.f, 1.f);
-                    const float a0 = __uint_as_float(r32[i]) * gv.x, a1 = __uint_as_float(r32[i + 1]) * gv.y;
-                    const float a2 = __uint_as_float(r32[i + 2]) * gv.z, a3 = __uint_as_float(r32[i + 3]) * gv.w;
-                    r32[i] = __float_as_uint(a0);
-                    r32[i + 1] = __float_as_uint(a1);
-                    r32[i + 2] = __float_as_uint(a2);
-                    r32[i + 3] = __float_as_uint(a3);
-                    r16[i / 2] = pack_bf16(a0 * gn.x, a1 * gn.y);
-                    r16[i / 2 + 1] = pack_bf16(a2 * gn.z, a3 * gn.w);
+                    const float4 gn = SM_AT(const float4, gnx + (32 * g4 + i) * 4);
+                    const float2 a01 = fmul2(make_float2(__uint_as_float(r32[i]), __uint_as_float(r32[i + 1])), make_float2(gv.x, gv.y));
+                    const float2 a23 = fmul2(make_float2(__uint_as_float(r32[i + 2]), __uint_as_float(r32[i + 3])), make_float2(gv.z, gv.w));
+                    r32[i] = __float_as_uint(a01.x);
+                    r32[i + 1] = __float_as_uint(a01.y);
+                    r32[i + 2] = __float_as_uint(a23.x);
+                    r32[i + 3] = __float_as_uint(a23.y);
+                    const float2 b01 = fmul2(a01, make_float2(gn.x, gn.y)), b23 = fmul2(a23, make_float2(gn.z, gn.w));
+                    r16[i / 2] = pack_bf16(b01.x, b01.y);
+                    r16[i / 2 + 1] = pack_bf16(b23.x, b23.y);
                 }
                 tc::st32(lb + T_S + 32 * g4, r32);
                 tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);

@@ -109,6 +109,18 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// ---------------------------------------------------------------- paired fp32
+// (a.x * b.x, a.y * b.y) as one f32x2 instruction
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // ---------------------------------------------------------------- packing
 // cvt.rn.{bf16,f16}x2.f32 d, a, b puts cvt(a) in the upper and cvt(b) in the lower half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
