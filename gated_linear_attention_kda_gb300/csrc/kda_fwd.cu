@@ -133,7 +133,7 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
 }
 
 static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
-                             const CUtensorMap &v, const CUtensorMap &g, const Params &p)
+                             const CUtensorMap &v, const CUtensorMap &g, const CUtensorMap &o, const Params &p)
 {
     static thread_local int configured_dev = -1;
     int dev = 0;
@@ -144,7 +144,7 @@ static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q,
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    tcs::kda_fwd_tc_kernel<<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    tcs::kda_fwd_tc_kernel<<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, o, p);
     return cudaGetLastError();
 }
 
@@ -216,14 +216,15 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
     if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)) || (cu_seqlens && !aligned(cu_seqlens, 8)))
         return fail(KDA_ERR_ALIGN, "A_log, dt_bias and cu_seqlens must be naturally aligned");
 
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mo;
+    std::memset(&mo, 0, sizeof mo);
     std::memset(&mq, 0, sizeof mq);
     std::memset(&mk, 0, sizeof mk);
     std::memset(&mv, 0, sizeof mv);
     std::memset(&mg, 0, sizeof mg);
     if (total > 0) {
         if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) || !make_map(&mv, v, total, H) ||
-            !make_map(&mg, g, total, H))
+            !make_map(&mg, g, total, H) || !make_map(&mo, out, total, H))
             return fail(KDA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad geometry)");
     }
     int dev = 0, nsm = 0;
@@ -253,7 +254,7 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
     p.vsplit = vs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (vs) {
-        case 1: ce = launch_tc(grid, s, mq, mk, mv, mg, p); break;
+        case 1: ce = launch_tc(grid, s, mq, mk, mv, mg, mo, p); break;
         case 2: ce = launch<4>(grid, s, mq, mk, mv, mg, p); break;
         case 4: ce = launch<2>(grid, s, mq, mk, mv, mg, p); break;
         default: ce = launch<1>(grid, s, mq, mk, mv, mg, p); break;

@@ -90,7 +90,8 @@ constexpr int SCR = S_AX + 2048;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_SLOT = OFF_RAW + NR * RAW_STAGE;
-constexpr int OFF_SCR = OFF_SLOT + NP * SLOT;
+constexpr int OFF_OST = OFF_SLOT + NP * SLOT;  // bf16 output tile [16 tokens][128], TMA-store layout
+constexpr int OFF_SCR = OFF_OST + RAW_TILE;
 constexpr int OFF_BAR = OFF_SCR + 2 * SCR;
 // barrier indices
 constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_PREP_FULL = 8, B_PREP_EMPTY = 12, B_D = 16, B_E = 18, B_G = 20,
@@ -104,7 +105,7 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(NR <= 4 && NP <= 4, "barrier index ranges");
 static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled operands need 1024-byte alignment");
 static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && S_AX % 16 == 0 && SCR % 16 == 0, "alignment");
-static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_OST % 1024 == 0, "mbarrier / swizzled tile alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
 // byte offset of (row n, col k) in a K-major, non-swizzled f16 operand with
@@ -155,7 +156,8 @@ __device__ __noinline__ void issue_d(uint32_t tmem, uint32_t sl, int dbuf, int b
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                      const __grid_constant__ CUtensorMap to, const Params p)
 {
     extern __shared__ uint8_t smem_dyn[];
     // align to 1024 B by pointer arithmetic on the shared array, so that accesses
@@ -341,13 +343,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc::fence_after();
-            uint32_t d[32];
-            tc::ld32(lb + T_D + 32 * (k % 3), d);
-            tc::wait_ld();
+            uint32_t o8[8];  // outputs as bf16 pairs, stored after the decay pass
             {  // E_k (f16) -> tensor memory, then release the chain
-                uint32_t e8[8];
+                uint32_t d[32], e8[8];
+                tc::ld32(lb + T_D + 32 * (k % 3), d);
+                tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) e8[i] = pack_f16(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+                for (int i = 0; i < 8; ++i) {
+                    e8[i] = pack_f16(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+                    o8[i] = pack_bf16(__uint_as_float(d[16 + 2 * i]), __uint_as_float(d[17 + 2 * i]));
+                }
                 tc::st8(lb + T_E + 8 * (k & 1), e8);
                 tc::wait_st();
                 tc::fence_before();
@@ -396,16 +401,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_G + (k & 1)));
-            // outputs (already scaled): one bf16 per token row, stepping by the token stride
+            // outputs (already scaled). Whole chunks go through a shared tile and one TMA store;
+            // a chunk cut short by the sequence end is stored row by row.
             const int Lv = min(CHUNK, sp.len - k * CHUNK);
-            uint16_t *op = p.out + (static_cast<size_t>(sp.bos + k * CHUNK) * p.H + h) * DH + row;
-            const size_t ostride = static_cast<size_t>(p.H) * DH;
+            const bool lead = warp == 2 && lane == 0;
+            if (Lv == CHUNK) {
+                if (lead) bulk_wait_read();  // the previous chunk's store has read the tile
+                named_bar_sync(3, 128);
 #pragma unroll
-            for (int r = 0; r < CHUNK; ++r) {
-                if (r < Lv) *op = f2bf_bits(__uint_as_float(d[16 + r]));
-                op += ostride;
+                for (int r = 0; r < CHUNK; ++r)
+                    SM_AT(uint16_t, sb + OFF_OST + raw_off(r, row)) = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
+                tc::fence_async_smem();
+                named_bar_sync(3, 128);
+                if (lead) {
+                    tma_store_3d(&to, sb + OFF_OST, 0, h, sp.bos + k * CHUNK);
+                    tma_store_3d(&to, sb + OFF_OST + RAW_BOX, 64, h, sp.bos + k * CHUNK);
+                    bulk_commit();
+                }
+            } else {
+                uint16_t *op = p.out + (static_cast<size_t>(sp.bos + k * CHUNK) * p.H + h) * DH + row;
+                const size_t ostride = static_cast<size_t>(p.H) * DH;
+#pragma unroll
+                for (int r = 0; r < CHUNK; ++r) {
+                    if (r < Lv) *op = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
+                    op += ostride;
+                }
             }
         }
+        if (warp == 2 && lane == 0) bulk_wait_all();
         if (p.fin) {
             if (ok && nch > 0) ok = wait_bar(bar(B_S + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1, flags);
             ok = __all_sync(0xffffffffu, ok);
