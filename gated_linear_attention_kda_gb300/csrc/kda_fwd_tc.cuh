@@ -62,7 +62,7 @@ constexpr uint32_t T_X = 384;   // X, 32 fp32 columns
 // prep slot (bytes)
 constexpr int L_Z = 0;         // bf16 Z, K-major 128B swizzle: 2 K-blocks x [32 rows][128 B]
 constexpr int L_V16 = 8192;    // f16 V, MN-major 128B swizzle: 2 boxes x [16 rows][128 B]
-constexpr int L_KB = 12288;    // f16 Kbar [128 n][16 k], K-major core matrices
+constexpr int L_KB = 12288;    // f16 Kbar [16 j][128 c], MN-major 128B swizzle (the raw-tile layout)
 constexpr int L_PHI = 16384;   // fp32 Phi [32 n][32 k], K-major core matrices (LBO 128, SBO 1024)
 constexpr int L_TM = 20480;    // f16 TM [32 n][16 k]
 constexpr int L_CC = 21504;    // f16 (H Phi^T)^T [32 n][16 k]
@@ -84,8 +84,8 @@ constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
 constexpr int S_TP = S_QG + 16 * H_LD;   // f16 T' [16][24]
 constexpr int S_PP = S_TP + 16 * M_LD;   // f16 P [16][24]
 constexpr int S_BETA = S_PP + 16 * M_LD; // fp32 beta [16]
-constexpr int S_GX = S_BETA + 64;        // fp32 [2][64][2]: gate sums between row halves; later s H^q fragments
-constexpr int S_AX = S_GX + 1024;        // fp32 [2][2][32 lanes][4]: second channel half of A and P
+constexpr int S_GX = S_BETA + 64;        // fp32 [2][32 lanes][4]: s H^q fragments
+constexpr int S_AX = S_GX + 1024;        // fp32 [4][32 lanes][4]: gate sums of the row quarters; later the second channel half of A and P
 constexpr int SCR = S_AX + 2048;
 
 constexpr int OFF_RAW = 0;
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0 && nch > 0) {
             const uint32_t id_c = tc::idesc(tc::F16, 128, 32, 0, 0);
-            const uint32_t id_s = tc::idesc(tc::F16, 128, 128, 0, 0);
+            const uint32_t id_s = tc::idesc(tc::F16, 128, 128, 0, 1);  // Kbar MN-major
             bool ok = wait_bar(bar(B_I), 0, flags);
             for (int n = 0; ok && n < (nch < 2 ? nch : 2); ++n) {
                 ok = wait_bar(bar(B_PREP_FULL + n % NP), (n / NP) & 1, flags);
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!ok) break;
                 tc::fence_after();
                 // S += E_k Kbar_k (the state was decayed in place by the state warps)
-                tc::mma_ts(tmem + T_S, e, tc::sdesc(slot(k) + L_KB, 128, 256, tc::SWZ_NONE), id_s, 1);
+                tc::mma_ts(tmem + T_S, e, tc::sdesc(slot(k) + L_KB, 2048, 1024, tc::SWZ_128B), id_s, 1);
                 tc::commit(bar(B_S + (k & 1)));
                 tc::commit(bar(B_PREP_EMPTY + k % NP));
                 if (k + 2 < nch) {
@@ -458,21 +458,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc::fence_before();
     } else {
         // ---------------------------------------------------------------- prep lanes
-        // lane = 4 warps = 128 threads. Element-wise passes: thread -> channel pair
-        // (c0, c0 + 1), rows [8 rh, 8 rh + 8).
+        // lane = 4 warps = 128 threads. Element-wise passes: thread -> channels
+        // [c0, c0 + 4) (c0 = 4 lane), rows [4 rq, 4 rq + 4) (row quarter rq = warp in lane).
         const int ln = (warp - 6) >> 2;
         const int lt = threadIdx.x - 192 - 128 * ln;  // 0..127
         const int lw = lt >> 5;
         const uint32_t bar_id = 1 + ln;
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
-        const int cp = lt & 63, rh = lt >> 6;
-        const int c0 = 2 * cp, r0 = 8 * rh;
+        const int rq = lw;
+        const int c0 = 4 * lane, r0 = 4 * rq;
         // x / 2 = ah2 * g + bb, with x = exp(A_log) (g + dt_bias)
-        float ah2 = 0.5f, bb0 = 0.f, bb1 = 0.f;
+        float ah2 = 0.5f, bb[4] = {0.f, 0.f, 0.f, 0.f};
         if (p.A_log) ah2 = 0.5f * ex2_approx(__ldg(p.A_log + h) * LOG2E);
         if (p.dt_bias) {
-            bb0 = ah2 * __ldg(p.dt_bias + h * DH + c0);
-            bb1 = ah2 * __ldg(p.dt_bias + h * DH + c0 + 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bb[j] = ah2 * __ldg(p.dt_bias + h * DH + c0 + j);
         }
         const float hs = p.half_gs, sc = p.scale;
         const int g = lane >> 2, t = lane & 3;
@@ -492,84 +492,104 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!wait_bar(bar(B_RAW_FULL + rs), (n / NR) & 1, flags)) failed = true;
             const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
 
-            // gate (log2 units) over this thread's 8 rows, local inclusive cumsum;
+            // gate (log2 units) over this thread's 4 rows x 4 channels, local inclusive cumsum;
             // rows past the chunk's end add nothing
-            float G0[8], G1[8];
+            float G[4][4];
             {
-                float a0 = 0.f, a1 = 0.f;
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     const int r = r0 + i;
-                    const uint32_t gw = SM_AT(const uint32_t, raw + OFF_G + raw_off(r, c0));
-                    const float t0 = tanh_approx(fmaf(ah2, bf16_lo(gw), bb0));
-                    const float t1 = tanh_approx(fmaf(ah2, bf16_hi(gw), bb1));
+                    const uint2 gw = SM_AT(const uint2, raw + OFF_G + raw_off(r, c0));
+                    const float gx[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
                     const bool live = r < Lv;
-                    a0 += live ? fmaf(hs, t0, hs) : 0.f;
-                    a1 += live ? fmaf(hs, t1, hs) : 0.f;
-                    G0[i] = a0;
-                    G1[i] = a1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float tj = tanh_approx(fmaf(ah2, gx[j], bb[j]));
+                        a[j] += live ? fmaf(hs, tj, hs) : 0.f;
+                        G[i][j] = a[j];
+                    }
                 }
             }
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
-            SM_AT(float2, scr + S_GX + rh * 512 + cp * 8) = make_float2(G0[7], G1[7]);
+            SM_AT(float4, scr + S_AX + rq * 512 + lane * 16) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
             if (lt < CHUNK)
                 SM_AT(float, scr + S_BETA + lt * 4) = lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
             named_bar_sync(bar_id, 128);
-            // Gm = G at row 7 (reference: halves the exponent range), Ge = G at row 15;
-            // d = G_r - Gm for this thread's rows
-            const float2 oth = SM_AT(const float2, scr + S_GX + (rh ^ 1) * 512 + cp * 8);
-            const float Gm0 = rh ? oth.x : G0[7], Gm1 = rh ? oth.y : G1[7];
-            const float Ge0 = rh ? oth.x + G0[7] : G0[7] + oth.x, Ge1 = rh ? oth.y + G1[7] : G1[7] + oth.y;
-            const float off0 = rh ? 0.f : Gm0, off1 = rh ? 0.f : Gm1;
-            const float gr0 = ex2_approx(Gm0), gr1 = ex2_approx(Gm1);            // 2^Gm
-            const float se0 = ex2_approx(Ge0 - Gm0), se1 = ex2_approx(Ge1 - Gm1);  // 2^(Ge - Gm)
-            if (rh) SM_AT(float2, sl + L_GAM + c0 * 4) = make_float2(ex2_approx(Ge0), ex2_approx(Ge1));
+            // quarter sums -> prefix before this quarter; Gm = G at row 7 (reference: halves the
+            // exponent range), Ge = G at row 15; d = G_r - Gm = G_local - (Gm - prefix)
+            float off[4], gr[4], se[4];
+            {
+                const float4 s0 = SM_AT(const float4, scr + S_AX + 0 * 512 + lane * 16);
+                const float4 s1 = SM_AT(const float4, scr + S_AX + 1 * 512 + lane * 16);
+                const float4 s2 = SM_AT(const float4, scr + S_AX + 2 * 512 + lane * 16);
+                const float4 s3 = SM_AT(const float4, scr + S_AX + 3 * 512 + lane * 16);
+                const float q0[4] = {s0.x, s0.y, s0.z, s0.w}, q1[4] = {s1.x, s1.y, s1.z, s1.w};
+                const float q2[4] = {s2.x, s2.y, s2.z, s2.w}, q3[4] = {s3.x, s3.y, s3.z, s3.w};
+                float ge[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float pre = rq == 0 ? 0.f : rq == 1 ? q0[j] : rq == 2 ? q0[j] + q1[j] : q0[j] + q1[j] + q2[j];
+                    const float gm = q0[j] + q1[j];
+                    ge[j] = gm + q2[j] + q3[j];
+                    off[j] = gm - pre;
+                    gr[j] = ex2_approx(gm);            // 2^Gm
+                    se[j] = ex2_approx(ge[j] - gm);    // 2^(Ge - Gm)
+                }
+                if (rq == 3)
+                    SM_AT(float4, sl + L_GAM + c0 * 4) =
+                        make_float4(ex2_approx(ge[0]), ex2_approx(ge[1]), ex2_approx(ge[2]), ex2_approx(ge[3]));
+            }
             // all raw loads first: stores below may alias them as far as the compiler knows
-            uint32_t kwv[8], qwv[8], vwv[8];
+            uint2 kwv[4], qwv[4], vwv[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 const int r = r0 + i;
-                const uint32_t kraw = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
-                kwv[i] = r < Lv ? kraw : 0u;  // keys past the chunk's end are zero
-                qwv[i] = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
-                vwv[i] = SM_AT(const uint32_t, raw + OFF_V + raw_off(r, c0));
+                const uint2 kraw = SM_AT(const uint2, raw + OFF_K + raw_off(r, c0));
+                kwv[i] = r < Lv ? kraw : make_uint2(0u, 0u);  // keys past the chunk's end are zero
+                qwv[i] = SM_AT(const uint2, raw + OFF_Q + raw_off(r, c0));
+                vwv[i] = SM_AT(const uint2, raw + OFF_V + raw_off(r, c0));
             }
-            float kb0[8], kb1[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 const int r = r0 + i;
-                const uint32_t kw = kwv[i], qw = qwv[i], vw = vwv[i];
-                const float d0 = G0[i] - off0, d1 = G1[i] - off1;
-                const float u0 = ex2_approx(d0), u1 = ex2_approx(d1);     // 2^(G_r - Gm)
-                const float f0 = ex2_approx(-d0), f1 = ex2_approx(-d1);   // 2^(Gm - G_r)
-                const float k0 = bf16_lo(kw), k1 = bf16_hi(kw), q0 = bf16_lo(qw), q1 = bf16_hi(qw);
-                const float kl0 = k0 * u0, kl1 = k1 * u1, ql0 = q0 * u0, ql1 = q1 * u1;
-                const float kr0 = k0 * f0, kr1 = k1 * f1;
-                const float kg0 = kl0 * gr0, kg1 = kl1 * gr1, qg0 = ql0 * gr0, qg1 = ql1 * gr1;  // K, Q * Gamma
+                const float k[4] = {bf16_lo(kwv[i].x), bf16_hi(kwv[i].x), bf16_lo(kwv[i].y), bf16_hi(kwv[i].y)};
+                const float q[4] = {bf16_lo(qwv[i].x), bf16_hi(qwv[i].x), bf16_lo(qwv[i].y), bf16_hi(qwv[i].y)};
+                float kl[4], ql[4], kr[4], kg[4], qg[4], kb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float d = G[i][j] - off[j];
+                    const float u = ex2_approx(d), f = ex2_approx(-d);  // 2^(G_r - Gm), 2^(Gm - G_r)
+                    kl[j] = k[j] * u;
+                    ql[j] = q[j] * u;
+                    kr[j] = k[j] * f;
+                    kg[j] = kl[j] * gr[j];  // K * Gamma
+                    qg[j] = ql[j] * gr[j];  // Q * Gamma
+                    kb[j] = kr[j] * se[j];  // Kbar = K * 2^(Ge - G_r)
+                }
                 const uint32_t o = r * H_LD + c0 * 2;
-                SM_AT(uint32_t, scr + S_KG + o) = pack_f16(kg0, kg1);
-                SM_AT(uint32_t, scr + S_QG + o) = pack_f16(qg0, qg1);
-                SM_AT(uint32_t, sl + L_Z + sw128_32rows(r, c0)) = pack_bf16(kg0, kg1);
-                SM_AT(uint32_t, sl + L_Z + sw128_32rows(16 + r, c0)) = pack_bf16(qg0, qg1);
-                SM_AT(uint32_t, sl + L_V16 + raw_off(r, c0)) = pack_f16(bf16_lo(vw), bf16_hi(vw));
-                uint32_t hi, lo;
-                split_bf16_trunc(kl0, kl1, hi, lo);
-                SM_AT(uint32_t, scr + S_KLH + o) = hi;
-                SM_AT(uint32_t, scr + S_KLL + o) = lo;
-                split_bf16_trunc(ql0, ql1, hi, lo);
-                SM_AT(uint32_t, scr + S_QLH + o) = hi;
-                SM_AT(uint32_t, scr + S_QLL + o) = lo;
-                split_bf16_trunc(kr0, kr1, hi, lo);
-                SM_AT(uint32_t, scr + S_KRH + o) = hi;
-                SM_AT(uint32_t, scr + S_KRL + o) = lo;
-                kb0[i] = kr0 * se0;
-                kb1[i] = kr1 * se1;
+                SM_AT(uint2, scr + S_KG + o) = make_uint2(pack_f16(kg[0], kg[1]), pack_f16(kg[2], kg[3]));
+                SM_AT(uint2, scr + S_QG + o) = make_uint2(pack_f16(qg[0], qg[1]), pack_f16(qg[2], qg[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(r, c0)) = make_uint2(pack_bf16(kg[0], kg[1]), pack_bf16(kg[2], kg[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(16 + r, c0)) = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
+                const uint2 vw = vwv[i];
+                SM_AT(uint2, sl + L_V16 + raw_off(r, c0)) = make_uint2(pack_f16(bf16_lo(vw.x), bf16_hi(vw.x)),
+                                                                       pack_f16(bf16_lo(vw.y), bf16_hi(vw.y)));
+                SM_AT(uint2, sl + L_KB + raw_off(r, c0)) = make_uint2(pack_f16(kb[0], kb[1]), pack_f16(kb[2], kb[3]));
+                uint32_t h0, l0, h1, l1;
+                split_bf16_trunc(kl[0], kl[1], h0, l0);
+                split_bf16_trunc(kl[2], kl[3], h1, l1);
+                SM_AT(uint2, scr + S_KLH + o) = make_uint2(h0, h1);
+                SM_AT(uint2, scr + S_KLL + o) = make_uint2(l0, l1);
+                split_bf16_trunc(ql[0], ql[1], h0, l0);
+                split_bf16_trunc(ql[2], ql[3], h1, l1);
+                SM_AT(uint2, scr + S_QLH + o) = make_uint2(h0, h1);
+                SM_AT(uint2, scr + S_QLL + o) = make_uint2(l0, l1);
+                split_bf16_trunc(kr[0], kr[1], h0, l0);
+                split_bf16_trunc(kr[2], kr[3], h1, l1);
+                SM_AT(uint2, scr + S_KRH + o) = make_uint2(h0, h1);
+                SM_AT(uint2, scr + S_KRL + o) = make_uint2(l0, l1);
             }
-            // Kbar = K * 2^(Ge - G_r) as the K-major [c][j] operand: one 16-byte row per channel
-            SM_AT(uint4, sl + L_KB + cm16(c0, r0)) = make_uint4(pack_f16(kb0[0], kb0[1]), pack_f16(kb0[2], kb0[3]),
-                                                               pack_f16(kb0[4], kb0[5]), pack_f16(kb0[6], kb0[7]));
-            SM_AT(uint4, sl + L_KB + cm16(c0 + 1, r0)) = make_uint4(pack_f16(kb1[0], kb1[1]), pack_f16(kb1[2], kb1[3]),
-                                                                   pack_f16(kb1[4], kb1[5]), pack_f16(kb1[6], kb1[7]));
             named_bar_sync(bar_id, 128);
             if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
 
@@ -644,9 +664,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t zt = scr + (lw == 1 ? S_KG : S_QG) + b_row;
 #pragma unroll
                     for (int kb = 0; kb < 8; ++kb) {
-                        const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));  // A rows j, k = c
                         uint32_t aK[4], bz[4];
-                        ldsm_x4_t(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
                         ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
                         mma_f16(hw.c[0], aK, bz[0], bz[1]);
                         mma_f16(hw.c[1], aK, bz[2], bz[3]);
@@ -663,9 +683,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int i = 0; i < 4; ++i) hp[i][0] = hp[i][1] = hp[i][2] = hp[i][3] = 0.f;
 #pragma unroll
                     for (int kb = 0; kb < 8; ++kb) {
-                        const uint32_t koff = (2 * kb + (mi >> 1)) * 256 + (mi & 1) * 128 + ri * 16;
+                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));  // A rows j, k = c
                         uint32_t aK[4], bk[4], bq[4];
-                        ldsm_x4_t(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
                         ldsm_x4(scr + S_KG + b_row + 32 * kb, bk[0], bk[1], bk[2], bk[3]);
                         ldsm_x4(scr + S_QG + b_row + 32 * kb, bq[0], bq[1], bq[2], bq[3]);
                         const float2 gl = SM_AT(const float2, prev + L_GAM + (16 * kb + 2 * t) * 4);
