@@ -143,15 +143,15 @@ __device__ __noinline__ void issue_d(uint32_t tmem, uint32_t sl, int dbuf, int b
     const uint32_t id_y = tc::idesc(tc::BF16, 128, 32, 0, 0);
     const uint32_t id_p = tc::idesc(tc::TF32, 128, 32, 0, 0);
     const uint32_t dn = tmem + T_D + 32 * dbuf, x = tmem + T_X;
+    // descriptors of the slot's operands, advanced by adding (byte offset >> 4) to the address field
+    const uint64_t dz = tc::sdesc(sl + L_Z, 16, 1024, tc::SWZ_128B), dp = tc::sdesc(sl + L_PHI, 128, 1024, tc::SWZ_NONE);
     tc::mma_ss(dn, tc::sdesc(sl + L_V16, 2048, 1024, tc::SWZ_128B), tc::sdesc(sl + L_TM, 128, 256, tc::SWZ_NONE), id_u, 0);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        tc::mma_ts(x, tmem + T_SB + 64 * b + 8 * i, tc::sdesc(sl + L_Z + (i >> 2) * 4096 + (i & 3) * 32, 16, 1024, tc::SWZ_128B),
-                   id_y, i > 0);
+        tc::mma_ts(x, tmem + T_SB + 64 * b + 8 * i, dz + (((i >> 2) * 4096 + (i & 3) * 32) >> 4), id_y, i > 0);
     if (e >= 0) tc::mma_ts(x, tmem + T_E + 8 * e, tc::sdesc(sl + L_HP, 128, 256, tc::SWZ_NONE), id_c, 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        tc::mma_ts_tf32(dn, x + 8 * i, tc::sdesc(sl + L_PHI + 256 * i, 128, 1024, tc::SWZ_NONE), id_p, 1);
+    for (int i = 0; i < 4; ++i) tc::mma_ts_tf32(dn, x + 8 * i, dp + ((256 * i) >> 4), id_p, 1);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
