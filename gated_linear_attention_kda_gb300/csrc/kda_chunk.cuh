@@ -156,4 +156,32 @@ __device__ __forceinline__ void chunk_gram_x3(uint32_t xh, uint32_t xl, uint32_t
         for (int i = 0; i < 4; ++i) acc.c[nt][i] += cross.c[nt][i];
 }
 
+// As chunk_gram_x3, with X rounded to bf16 once and R as hi + lo: two bf16 products
+// X Rh + X Rl per entry (R keeps ~16-bit precision, X 8 bits).
+template <int NK>
+__device__ __forceinline__ void chunk_gram_x2(uint32_t x, uint32_t rh, uint32_t rl, Frag16 &acc, int lane, int kbase)
+{
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint32_t aoff = (ri + 8 * (mi & 1)) * 272 + 16 * (mi >> 1) + 32 * kbase;
+    const uint32_t boff = (ri + 8 * (mi >> 1)) * 272 + 16 * (mi & 1) + 32 * kbase;
+    Frag16 cross;
+    frag_zero(acc);
+    frag_zero(cross);
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+        uint32_t a[4], bh[4], bl[4];
+        ldsm_x4(x + aoff + 32 * kk, a[0], a[1], a[2], a[3]);
+        ldsm_x4(rh + boff + 32 * kk, bh[0], bh[1], bh[2], bh[3]);
+        ldsm_x4(rl + boff + 32 * kk, bl[0], bl[1], bl[2], bl[3]);
+        mma_bf16(acc.c[0], a, bh[0], bh[1]);
+        mma_bf16(acc.c[1], a, bh[2], bh[3]);
+        mma_bf16(cross.c[0], a, bl[0], bl[1]);
+        mma_bf16(cross.c[1], a, bl[2], bl[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc.c[nt][i] += cross.c[nt][i];
+}
+
 }  // namespace kda

@@ -576,15 +576,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 SM_AT(uint2, sl + L_V16 + raw_off(r, c0)) = make_uint2(pack_f16(bf16_lo(vw.x), bf16_hi(vw.x)),
                                                                        pack_f16(bf16_lo(vw.y), bf16_hi(vw.y)));
                 SM_AT(uint2, sl + L_KB + raw_off(r, c0)) = make_uint2(pack_f16(kb[0], kb[1]), pack_f16(kb[2], kb[3]));
+                SM_AT(uint2, scr + S_KLH + o) = make_uint2(pack_bf16(kl[0], kl[1]), pack_bf16(kl[2], kl[3]));
+                SM_AT(uint2, scr + S_QLH + o) = make_uint2(pack_bf16(ql[0], ql[1]), pack_bf16(ql[2], ql[3]));
                 uint32_t h0, l0, h1, l1;
-                split_bf16_trunc(kl[0], kl[1], h0, l0);
-                split_bf16_trunc(kl[2], kl[3], h1, l1);
-                SM_AT(uint2, scr + S_KLH + o) = make_uint2(h0, h1);
-                SM_AT(uint2, scr + S_KLL + o) = make_uint2(l0, l1);
-                split_bf16_trunc(ql[0], ql[1], h0, l0);
-                split_bf16_trunc(ql[2], ql[3], h1, l1);
-                SM_AT(uint2, scr + S_QLH + o) = make_uint2(h0, h1);
-                SM_AT(uint2, scr + S_QLL + o) = make_uint2(l0, l1);
                 split_bf16_trunc(kr[0], kr[1], h0, l0);
                 split_bf16_trunc(kr[2], kr[3], h1, l1);
                 SM_AT(uint2, scr + S_KRH + o) = make_uint2(h0, h1);
@@ -594,12 +588,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
 
             // A (warps 0, 2) and P (warps 1, 3), each warp over one channel half;
-            // three bf16 products per entry (hi/lo split)
+            // two bf16 products per entry: Kl, Ql rounded once, Kr as hi + lo
             const bool isP = lw & 1;
             const int khalf = lw >> 1;
             Frag16 acc;
-            chunk_gram_x3<4>(scr + (isP ? S_QLH : S_KLH), scr + (isP ? S_QLL : S_KLL), scr + S_KRH, scr + S_KRL, acc, lane,
-                             4 * khalf);
+            chunk_gram_x2<4>(scr + (isP ? S_QLH : S_KLH), scr + S_KRH, scr + S_KRL, acc, lane, 4 * khalf);
             {
                 const uint32_t xa = scr + S_AX + (isP ? 1024 : 0) + lane * 16;
                 if (khalf) {
