@@ -186,13 +186,9 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
                 SM_AT(uint32_t, pslot + P_KB + r * BZ_LD + c0 * 2) = pack_f16(k0 * f0 * se0, k1 * f1 * se1);
                 const float u0 = gm0 * sm0, u1 = gm1 * sm1;                              // 2^(G_r - G_mid)
                 const uint32_t o = r * H_LD + c0 * 2;
+                SM_AT(uint32_t, scr + S_KLH + o) = pack_bf16(k0 * u0, k1 * u1);
+                SM_AT(uint32_t, scr + S_QLH + o) = pack_bf16(q0 * u0, q1 * u1);
                 uint32_t hi, lo;
-                split_bf16(k0 * u0, k1 * u1, hi, lo);
-                SM_AT(uint32_t, scr + S_KLH + o) = hi;
-                SM_AT(uint32_t, scr + S_KLL + o) = lo;
-                split_bf16(q0 * u0, q1 * u1, hi, lo);
-                SM_AT(uint32_t, scr + S_QLH + o) = hi;
-                SM_AT(uint32_t, scr + S_QLL + o) = lo;
                 split_bf16(k0 * f0, k1 * f1, hi, lo);
                 SM_AT(uint32_t, scr + S_KRH + o) = hi;
                 SM_AT(uint32_t, scr + S_KRL + o) = lo;
@@ -203,13 +199,13 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
             if (lt == 0) mbar_arrive(raw_empty + 8 * rs);
 
             // warp 0: A = strictly-lower(beta_r Kl Kr^T), T' = (I + A)^-1 diag(beta);
-            // warp 1: P = lower(Ql Kr^T). Three bf16 products per entry (hi/lo split).
+            // warp 1: P = lower(Ql Kr^T). Two bf16 products per entry: Kl, Ql rounded once, Kr as hi + lo.
             {
                 Frag16 acc;
                 if (lw == 0)
-                    chunk_gram_x3<8>(scr + S_KLH, scr + S_KLL, scr + S_KRH, scr + S_KRL, acc, lane, 0);
+                    chunk_gram_x2<8>(scr + S_KLH, scr + S_KRH, scr + S_KRL, acc, lane, 0);
                 else
-                    chunk_gram_x3<8>(scr + S_QLH, scr + S_QLL, scr + S_KRH, scr + S_KRL, acc, lane, 0);
+                    chunk_gram_x2<8>(scr + S_QLH, scr + S_KRH, scr + S_KRL, acc, lane, 0);
                 if (lw == 0) {
                     const float bg = SM_AT(const float, scr + S_BETA + g * 4), bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
 #pragma unroll
