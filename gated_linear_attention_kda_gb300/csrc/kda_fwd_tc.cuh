@@ -84,7 +84,7 @@ constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
 constexpr int S_TP = S_QG + 16 * H_LD;   // f16 T' [16][24]
 constexpr int S_PP = S_TP + 16 * M_LD;   // f16 P [16][24]
 constexpr int S_BETA = S_PP + 16 * M_LD; // fp32 beta [16]
-constexpr int S_GX = S_BETA + 64;        // fp32 [2][32 lanes][4]: s H^q fragments
+constexpr int S_GX = S_BETA + 64;        // [32 lanes][4 words]: H^w as an f16 A fragment
 constexpr int S_AX = S_GX + 1024;        // fp32 [4][32 lanes][4]: gate sums of the row quarters; later the second channel half of A and P
 constexpr int SCR = S_AX + 2048;
 
@@ -479,16 +479,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int mi = lane >> 3, ri = lane & 7;
         // B operand (n = tile row, k = tile column) of a row-major [16][136] 16-bit tile
         const uint32_t b_row = (ri + 8 * (mi >> 1)) * H_LD + 16 * (mi & 1);
+        // transposed fragment stores into a [32 n][16 k] K-major core-matrix tile: lane 8 mi + ri
+        // addresses row ri of the core matrix (n block mi >> 1, k block mi & 1)
+        const uint32_t stsm_row = (mi >> 1) * 256 + (mi & 1) * 128 + ri * 16;
 
+        // bf16 bits of the beta logit of row lt of chunk n, loaded one lane-chunk ahead and
+        // left untouched until used (rows past the sequence end read its last row and are
+        // masked where they are used)
+        auto beta_bits = [&](int n) -> uint32_t {
+            if (lt >= CHUNK) return 0u;
+            const int r = min(n * CHUNK + lt, sp.len - 1);
+            return __ldg(p.beta + static_cast<size_t>(sp.bos + r) * p.H + h);
+        };
+        uint32_t bnext = ln < nch ? beta_bits(ln) : 0u;
         for (int n = ln; n < nch; n += 2) {
             bool failed = false;
             const int rs = n % NR;
             const uint32_t sl = slot(n);
-            const int tok0 = sp.bos + n * CHUNK;
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
-            float blogit = 0.f;
-            if (lt < Lv)
-                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lt) * p.H + h)) << 16);
+            const uint32_t bbits = bnext;
+            if (n + 2 < nch) bnext = beta_bits(n + 2);
             if (!wait_bar(bar(B_RAW_FULL + rs), (n / NR) & 1, flags)) failed = true;
             const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
 
@@ -514,7 +524,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
             SM_AT(float4, scr + S_AX + rq * 512 + lane * 16) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
             if (lt < CHUNK)
-                SM_AT(float, scr + S_BETA + lt * 4) = lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * blogit), 0.5f) : 0.f;
+                SM_AT(float, scr + S_BETA + lt * 4) = lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * __uint_as_float(bbits << 16)), 0.5f) : 0.f;
             named_bar_sync(bar_id, 128);
             // quarter sums -> prefix before this quarter; Gm = G at row 7 (reference: halves the
             // exponent range), Ge = G at row 15; d = G_r - Gm = G_local - (Gm - prefix)
@@ -664,10 +674,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         mma_f16(hw.c[0], aK, bz[0], bz[1]);
                         mma_f16(hw.c[1], aK, bz[2], bz[3]);
                     }
-                    if (lw == 2) {  // s H^q for warp 1
-                        const uint32_t xh = scr + S_GX + lane * 16;
-                        SM_AT(float4, xh) = make_float4(sc * hw.c[0][0], sc * hw.c[0][1], sc * hw.c[0][2], sc * hw.c[0][3]);
-                        SM_AT(float4, xh + 512) = make_float4(sc * hw.c[1][0], sc * hw.c[1][1], sc * hw.c[1][2], sc * hw.c[1][3]);
+                    if (lw == 1) {  // H^w as an f16 A fragment, for warp 2's half of the correction
+                        uint32_t aH[4];
+                        frag_as_a(hw, aH);
+                        SM_AT(uint4, scr + S_GX + lane * 16) = make_uint4(aH[0], aH[1], aH[2], aH[3]);
                     }
                 } else {
                     // H'' = Kbar_{n-2} Diag(gamma_{n-1}) Z^T (16 x 32), stored as [n = column][k = j]
@@ -690,19 +700,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         mma_f16(hp[3], aK, hmul2(bq[2], gk0), hmul2(bq[3], gk1));
                     }
 #pragma unroll
-                    for (int nu = 0; nu < 4; ++nu)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int j = g + 8 * (i >> 1), col = 8 * nu + 2 * t + (i & 1);
-                            SM_AT(uint16_t, sl + L_HP + cm16(col, j)) = f2h_bits(hp[nu][i]);
-                        }
+                    for (int nu = 0; nu < 4; nu += 2)
+                        stsm_x4_t(sl + L_HP + nu * 256 + stsm_row, pack_f16(hp[nu][0], hp[nu][1]), pack_f16(hp[nu][2], hp[nu][3]),
+                                  pack_f16(hp[nu + 1][0], hp[nu + 1][1]), pack_f16(hp[nu + 1][2], hp[nu + 1][3]));
                 }
             }
             named_bar_sync(bar_id, 128);
 
-            // M = P T' (warps 0, 1): warp 0 writes TM rows 16..31 = s M and Phi rows 16..31 =
-            // [-s M, s I]; warp 1 writes (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q]
-            if (lw < 2) {
+            // M = P T' (warps 0, 2). Warp 0 writes TM rows 16..31 = s M and Phi rows 16..31 =
+            // [-s M, s I]; (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q] is written by
+            // warp 1 (first 16 columns) and warp 2 (last 16)
+            if (lw == 1) {
+                uint32_t aH[4];
+                frag_as_a(hw, aH);
+                // B[k = m][n] = -T'[n][m]: the T' tile rows are n
+                uint32_t bt[4];
+                ldsm_x4(scr + S_TP + (ri + 8 * (mi >> 1)) * M_LD + 16 * (mi & 1), bt[0], bt[1], bt[2], bt[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) bt[i] ^= 0x80008000u;
+                float cf[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
+                mma_f16(cf[0], aH, bt[0], bt[1]);
+                mma_f16(cf[1], aH, bt[2], bt[3]);
+                stsm_x4_t(sl + L_CC + stsm_row, pack_f16(cf[0][0], cf[0][1]), pack_f16(cf[0][2], cf[0][3]),
+                          pack_f16(cf[1][0], cf[1][1]), pack_f16(cf[1][2], cf[1][3]));
+            } else if (lw != 3) {
                 uint32_t aP[4], b0, b1, b2, b3;
                 ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
                 ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
@@ -730,33 +753,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 make_float2(r == col ? sc : 0.f, r == col + 1 ? sc : 0.f);
                         }
                 } else {
-                    // A operand: H^w (rows j, k = m)
-                    uint32_t aH[4];
-                    frag_as_a(hw, aH);
-                    float cf[4][4];
+                    // A operand: H^w from warp 1; B[k = m][n = i] = -s M[i][m], from the fragments of M
+                    const uint4 ah = SM_AT(const uint4, scr + S_GX + lane * 16);
+                    const uint32_t aH[4] = {ah.x, ah.y, ah.z, ah.w};
+                    float cf[2][4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
-                    // B[k = m][n] = -T'[n][m]: the T' tile rows are n
-                    uint32_t bt[4];
-                    ldsm_x4(scr + S_TP + (ri + 8 * (mi >> 1)) * M_LD + 16 * (mi & 1), bt[0], bt[1], bt[2], bt[3]);
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) bt[i] ^= 0x80008000u;
-                    mma_f16(cf[0], aH, bt[0], bt[1]);
-                    mma_f16(cf[1], aH, bt[2], bt[3]);
-                    // B[k = m][n = i] = -s M[i][m], from the accumulator fragments of M
-                    mma_f16(cf[2], aH, sm16[0][0] ^ 0x80008000u, sm16[1][0] ^ 0x80008000u);
-                    mma_f16(cf[3], aH, sm16[0][1] ^ 0x80008000u, sm16[1][1] ^ 0x80008000u);
-                    const uint32_t xh = scr + S_GX + lane * 16;
-                    const float4 q0 = SM_AT(const float4, xh), q1 = SM_AT(const float4, xh + 512);
-                    cf[2][0] += q0.x; cf[2][1] += q0.y; cf[2][2] += q0.z; cf[2][3] += q0.w;
-                    cf[3][0] += q1.x; cf[3][1] += q1.y; cf[3][2] += q1.z; cf[3][3] += q1.w;
+                        for (int i = 0; i < 4; ++i) cf[nt][i] = 0.f;
+                    mma_f16(cf[0], aH, sm16[0][0] ^ 0x80008000u, sm16[1][0] ^ 0x80008000u);
+                    mma_f16(cf[1], aH, sm16[0][1] ^ 0x80008000u, sm16[1][1] ^ 0x80008000u);
 #pragma unroll
-                    for (int nu = 0; nu < 4; ++nu)
+                    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int j = g + 8 * (i >> 1), col = 8 * nu + 2 * t + (i & 1);
-                            SM_AT(uint16_t, sl + L_CC + cm16(col, j)) = f2h_bits(cf[nu][i]);
-                        }
+                        for (int i = 0; i < 4; ++i) cf[nt][i] += sc * hw.c[nt][i];  // + s H^q (this warp's product)
+                    stsm_x4_t(sl + L_CC + 512 + stsm_row, pack_f16(cf[0][0], cf[0][1]), pack_f16(cf[0][2], cf[0][3]),
+                              pack_f16(cf[1][0], cf[1][1]), pack_f16(cf[1][2], cf[1][3]));
                 }
             }
             tc::fence_async_smem();

@@ -90,8 +90,12 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // every committed bulk store has completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// bar.sync / bar.red are the .aligned barrier forms: every thread of a warp must
+// execute them together, so each wrapper first reconverges the warp (a waiting
+// loop or a single-lane branch before the barrier may have split it).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
@@ -99,6 +103,7 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 // every participant receives the same result.
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred)
 {
+    __syncwarp();
     uint32_t r;
     asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
                  "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
@@ -232,6 +237,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(a));
+}
+
+// stmatrix, transposed: lane 8 i + r gives the address of memory row r of
+// matrix i, which receives column r of that matrix's m16n8-style fragment.
+__device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3)
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- warp MMA
