@@ -50,7 +50,7 @@ namespace tcs {
 
 constexpr int NR = 3;  // raw chunk ring
 constexpr int NP = 4;  // prep slot ring
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 512;
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;     // fp32 state, 128 columns
@@ -72,21 +72,18 @@ constexpr int SLOT = 24576;
 
 // prep scratch (per lane); 16-bit tiles are [16][136] (272-byte rows)
 constexpr int H_LD = 272;
-constexpr int M_LD = 48;   // 16-bit [16][24]
-constexpr int S_KLH = 0;   // bf16 hi/lo of K * 2^(G - G_mid), Q * 2^(G - G_mid), K * 2^(G_mid - G)
-constexpr int S_KLL = S_KLH + 16 * H_LD;
-constexpr int S_QLH = S_KLL + 16 * H_LD;
-constexpr int S_QLL = S_QLH + 16 * H_LD;
-constexpr int S_KRH = S_QLL + 16 * H_LD;
+constexpr int S_KLH = 0;                 // bf16 K * 2^(G - G_mid)
+constexpr int S_QLH = S_KLH + 16 * H_LD; // bf16 Q * 2^(G - G_mid)
+constexpr int S_KRH = S_QLH + 16 * H_LD; // bf16 hi / lo of K * 2^(G_mid - G)
 constexpr int S_KRL = S_KRH + 16 * H_LD;
 constexpr int S_KG = S_KRL + 16 * H_LD;  // f16 K * Gamma
 constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
-constexpr int S_TP = S_QG + 16 * H_LD;   // f16 T' [16][24]
-constexpr int S_PP = S_TP + 16 * M_LD;   // f16 P [16][24]
-constexpr int S_BETA = S_PP + 16 * M_LD; // fp32 beta [16]
-constexpr int S_GX = S_BETA + 64;        // [32 lanes][4 words]: H^w as an f16 A fragment
-constexpr int S_AX = S_GX + 1024;        // fp32 [4][32 lanes][4]: gate sums of the row quarters; later the second channel half of A and P
-constexpr int SCR = S_AX + 2048;
+// handed to the lane's finisher warp, two buffers (alternate chunks of the lane)
+constexpr int S_BETA = S_QG + 16 * H_LD; // fp32 [2][16] beta
+constexpr int S_GP = S_BETA + 128;       // fp32 [2][4 warps][2 tiles][32 lanes][4]: A (warps 0, 2) and P (1, 3) partial
+                                         // sums; before them the chunk's gate sums [4 row quarters][32 lanes][4]
+constexpr int S_HX = S_GP + 2 * 4096;    // [2][H^w as an f16 A fragment (32 lanes x 16 B) | H^q fragments (2 x 32 lanes x 16 B)]
+constexpr int SCR = S_HX + 2 * 1536;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_SLOT = OFF_RAW + NR * RAW_STAGE;
@@ -95,16 +92,15 @@ constexpr int OFF_SCR = OFF_OST + RAW_TILE;
 constexpr int OFF_BAR = OFF_SCR + 2 * SCR;
 // barrier indices
 constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_PREP_FULL = 8, B_PREP_EMPTY = 12, B_D = 16, B_E = 18, B_G = 20,
-              B_S = 22, B_I = 24, B_F = 25, NBARS = 26;
-constexpr int OFF_ONES = OFF_BAR + NBARS * 8;  // fp32 [128] of 1.0: gamma after the last chunk
-constexpr int OFF_TMEMPTR = OFF_ONES + DH * 4;
+              B_S = 22, B_I = 24, B_F = 25, B_P2 = 26, B_GRAM = 30, B_HRDY = 34, B_FDONE = 38, B_GAM = 42, NBARS = 46;
+constexpr int OFF_TMEMPTR = OFF_BAR + NBARS * 8;
 constexpr int OFF_FLAGS = OFF_TMEMPTR + 16;
 constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 
-static_assert(NR <= 4 && NP <= 4, "barrier index ranges");
+static_assert(NR <= 4 && NP == 4, "barrier index ranges");
 static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled operands need 1024-byte alignment");
-static_assert(S_KG % 16 == 0 && S_TP % 16 == 0 && S_PP % 16 == 0 && S_AX % 16 == 0 && SCR % 16 == 0, "alignment");
+static_assert(S_KG % 16 == 0 && S_GP % 16 == 0 && S_HX % 16 == 0 && SCR % 16 == 0, "alignment");
 static_assert(OFF_BAR % 8 == 0 && OFF_OST % 1024 == 0, "mbarrier / swizzled tile alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -191,7 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < NP; ++i) {
             mbar_init(bar(B_PREP_FULL + i), 1);
-            mbar_init(bar(B_PREP_EMPTY + i), 2);
+            mbar_init(bar(B_PREP_EMPTY + i), 1 + 128);  // the state update's commit + the lane reading it two chunks later
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_D + i), 1);
@@ -201,10 +197,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mbar_init(bar(B_I), 4);
         mbar_init(bar(B_F), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(B_P2 + i), 1);
+            mbar_init(bar(B_GAM + i), 32);
+            mbar_init(bar(B_GRAM + i), 128);
+            mbar_init(bar(B_HRDY + i), 128);
+            mbar_init(bar(B_FDONE + i), 1);
+        }
         flags[0] = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < DH) SM_AT(float, sb + OFF_ONES + threadIdx.x * 4) = 1.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -282,13 +284,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = 32 * q4 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const size_t st_row = (static_cast<size_t>(seq) * p.H + h) * (DH * DH) + static_cast<size_t>(row) * DH;
-        // S_0, bf16(S_0) for chunk 0's product and bf16(S_0 Diag(gamma_0)) for chunk 1's
-        bool ok = nch == 0 || wait_bar(bar(B_PREP_FULL + 0), 0, flags);
-        ok = __all_sync(0xffffffffu, ok);
-        tc::fence_after();
+        // S_0, and bf16(S_0) for the products of chunks 0 and 1 (chunk 1's Z carries gamma_0)
+        bool ok = true;
 #pragma unroll 1
         for (int g4 = 0; g4 < 4; ++g4) {
-            uint32_t r32[32], r16[16], r16g[16];
+            uint32_t r32[32], r16[16];
             if (!p.init) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r32[i] = 0u;
@@ -318,18 +318,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const float4 g0 = nch > 0 ? SM_AT(const float4, slot(0) + L_GAM + (32 * g4 + i) * 4) : make_float4(1.f, 1.f, 1.f, 1.f);
-                const float x0 = __uint_as_float(r32[i]), x1 = __uint_as_float(r32[i + 1]);
-                const float x2 = __uint_as_float(r32[i + 2]), x3 = __uint_as_float(r32[i + 3]);
-                r16[i / 2] = pack_bf16(x0, x1);
-                r16[i / 2 + 1] = pack_bf16(x2, x3);
-                r16g[i / 2] = pack_bf16(x0 * g0.x, x1 * g0.y);
-                r16g[i / 2 + 1] = pack_bf16(x2 * g0.z, x3 * g0.w);
-            }
+            for (int i = 0; i < 32; i += 2) r16[i / 2] = pack_bf16(__uint_as_float(r32[i]), __uint_as_float(r32[i + 1]));
             tc::st32(lb + T_S + 32 * g4, r32);
             tc::st16(lb + T_SB + 16 * g4, r16);
-            tc::st16(lb + T_SB + 64 + 16 * g4, r16g);
+            tc::st16(lb + T_SB + 64 + 16 * g4, r16);
         }
         tc::wait_st();
         tc::fence_before();
@@ -359,33 +351,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_E + (k & 1)));
             }
-            // decay the state for this chunk, S <- S Diag(gamma_k), and keep
-            // bf16(S Diag(gamma_k gamma_{k+1})) for chunk k + 2's product
-            const bool more = k + 1 < nch;
+            // decay the state for this chunk, S <- S Diag(gamma_k), and keep bf16 of it for
+            // chunk k + 2's product (whose Z carries gamma_{k+1})
             ok = (k == 0) || wait_bar(bar(B_S + ((k - 1) & 1)), ((k - 1) >> 1) & 1, flags);
             ok = ok && wait_bar(bar(B_PREP_FULL + k % NP), (k / NP) & 1, flags);
-            ok = ok && (!more || wait_bar(bar(B_PREP_FULL + (k + 1) % NP), ((k + 1) / NP) & 1, flags));
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after();
-            const uint32_t gam = slot(k) + L_GAM, gnx = more ? slot(k + 1) + L_GAM : sb + OFF_ONES;
+            const uint32_t gam = slot(k) + L_GAM;
             auto decay_block = [&](int g4, uint32_t(&r32)[32]) {
                 uint32_t r16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
-                    const float4 gn = SM_AT(const float4, gnx + (32 * g4 + i) * 4);
                     const float2 a01 = fmul2(make_float2(__uint_as_float(r32[i]), __uint_as_float(r32[i + 1])), make_float2(gv.x, gv.y));
                     const float2 a23 = fmul2(make_float2(__uint_as_float(r32[i + 2]), __uint_as_float(r32[i + 3])), make_float2(gv.z, gv.w));
                     r32[i] = __float_as_uint(a01.x);
                     r32[i + 1] = __float_as_uint(a01.y);
                     r32[i + 2] = __float_as_uint(a23.x);
                     r32[i + 3] = __float_as_uint(a23.y);
-                    const float2 b01 = fmul2(a01, make_float2(gn.x, gn.y)), b23 = fmul2(a23, make_float2(gn.z, gn.w));
-                    r16[i / 2] = pack_bf16(b01.x, b01.y);
-                    r16[i / 2 + 1] = pack_bf16(b23.x, b23.y);
+                    r16[i / 2] = pack_bf16(a01.x, a01.y);
+                    r16[i / 2 + 1] = pack_bf16(a23.x, a23.y);
                 }
                 tc::st32(lb + T_S + 32 * g4, r32);
                 tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);
@@ -456,10 +444,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         tc::fence_before();
-    } else {
+    } else if (warp < 14) {
         // ---------------------------------------------------------------- prep lanes
-        // lane = 4 warps = 128 threads. Element-wise passes: thread -> channels
-        // [c0, c0 + 4) (c0 = 4 lane), rows [4 rq, 4 rq + 4) (row quarter rq = warp in lane).
+        // lane = 4 warps = 128 threads, alternate chunks. Element-wise passes: thread ->
+        // channels [c0, c0 + 4) (c0 = 4 lane), rows [4 rq, 4 rq + 4) (row quarter rq = warp
+        // in lane). The lane forms the gate, the scaled key / query tiles, the chunk-product
+        // partial sums and the cross-chunk products; its finisher warp does the rest.
         const int ln = (warp - 6) >> 2;
         const int lt = threadIdx.x - 192 - 128 * ln;  // 0..127
         const int lw = lt >> 5;
@@ -474,8 +464,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) bb[j] = ah2 * __ldg(p.dt_bias + h * DH + c0 + j);
         }
-        const float hs = p.half_gs, sc = p.scale;
-        const int g = lane >> 2, t = lane & 3;
+        const float hs = p.half_gs;
+        const int t = lane & 3;
         const int mi = lane >> 3, ri = lane & 7;
         // B operand (n = tile row, k = tile column) of a row-major [16][136] 16-bit tile
         const uint32_t b_row = (ri + 8 * (mi >> 1)) * H_LD + 16 * (mi & 1);
@@ -492,13 +482,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return __ldg(p.beta + static_cast<size_t>(sp.bos + r) * p.H + h);
         };
         uint32_t bnext = ln < nch ? beta_bits(ln) : 0u;
+        bool failed = false;  // sticky: a wait gave up; OR-reduced at the lane barriers
         for (int n = ln; n < nch; n += 2) {
-            bool failed = false;
             const int rs = n % NR;
             const uint32_t sl = slot(n);
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
             const uint32_t bbits = bnext;
             if (n + 2 < nch) bnext = beta_bits(n + 2);
+            const int xb = (n >> 1) & 1;                        // finisher buffer of this chunk
+            const uint32_t xpar = static_cast<uint32_t>(n >> 2) & 1;
             if (!wait_bar(bar(B_RAW_FULL + rs), (n / NR) & 1, flags)) failed = true;
             const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
 
@@ -522,18 +514,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
-            SM_AT(float4, scr + S_AX + rq * 512 + lane * 16) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
+            // the finisher is done with this buffer's previous chunk
+            if (!wait_bar(bar(B_FDONE + 2 * ln + xb), xpar ^ 1, flags)) failed = true;
+            // gate sums of the row quarters, in this chunk's partial-sum buffer (free until the products)
+            const uint32_t gsum = scr + S_GP + xb * 4096;
+            SM_AT(float4, gsum + rq * 512 + lane * 16) = make_float4(G[3][0], G[3][1], G[3][2], G[3][3]);
             if (lt < CHUNK)
-                SM_AT(float, scr + S_BETA + lt * 4) = lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * __uint_as_float(bbits << 16)), 0.5f) : 0.f;
-            named_bar_sync(bar_id, 128);
+                SM_AT(float, scr + S_BETA + xb * 64 + lt * 4) =
+                    lt < Lv ? fmaf(0.5f, tanh_approx(0.5f * __uint_as_float(bbits << 16)), 0.5f) : 0.f;
+            if (named_bar_or(bar_id, 128, failed)) break;
             // quarter sums -> prefix before this quarter; Gm = G at row 7 (reference: halves the
             // exponent range), Ge = G at row 15; d = G_r - Gm = G_local - (Gm - prefix)
             float off[4], gr[4], se[4];
             {
-                const float4 s0 = SM_AT(const float4, scr + S_AX + 0 * 512 + lane * 16);
-                const float4 s1 = SM_AT(const float4, scr + S_AX + 1 * 512 + lane * 16);
-                const float4 s2 = SM_AT(const float4, scr + S_AX + 2 * 512 + lane * 16);
-                const float4 s3 = SM_AT(const float4, scr + S_AX + 3 * 512 + lane * 16);
+                const float4 s0 = SM_AT(const float4, gsum + 0 * 512 + lane * 16);
+                const float4 s1 = SM_AT(const float4, gsum + 1 * 512 + lane * 16);
+                const float4 s2 = SM_AT(const float4, gsum + 2 * 512 + lane * 16);
+                const float4 s3 = SM_AT(const float4, gsum + 3 * 512 + lane * 16);
                 const float q0[4] = {s0.x, s0.y, s0.z, s0.w}, q1[4] = {s1.x, s1.y, s1.z, s1.w};
                 const float q2[4] = {s2.x, s2.y, s2.z, s2.w}, q3[4] = {s3.x, s3.y, s3.z, s3.w};
                 float ge[4];
@@ -546,9 +543,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     gr[j] = ex2_approx(gm);            // 2^Gm
                     se[j] = ex2_approx(ge[j] - gm);    // 2^(Ge - Gm)
                 }
-                if (rq == 3)
+                if (rq == 3) {
                     SM_AT(float4, sl + L_GAM + c0 * 4) =
                         make_float4(ex2_approx(ge[0]), ex2_approx(ge[1]), ex2_approx(ge[2]), ex2_approx(ge[3]));
+                    mbar_arrive(bar(B_GAM + n % NP));
+                }
+            }
+            // gamma_{n-1} of this thread's channels (the previous chunk, the other lane): the state
+            // product of chunk n reads Z_n Diag(gamma_{n-1}) against the state decayed to the start
+            // of chunk n-1, so Z is stored pre-scaled (gamma_{-1} = 1)
+            float gp[4] = {1.f, 1.f, 1.f, 1.f};
+            if (n >= 1) {
+                if (!wait_bar(bar(B_GAM + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+                const float4 gv = SM_AT(const float4, slot(n + NP - 1) + L_GAM + c0 * 4);
+                gp[0] = gv.x; gp[1] = gv.y; gp[2] = gv.z; gp[3] = gv.w;
             }
             // all raw loads first: stores below may alias them as far as the compiler knows
             uint2 kwv[4], qwv[4], vwv[4];
@@ -580,8 +588,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t o = r * H_LD + c0 * 2;
                 SM_AT(uint2, scr + S_KG + o) = make_uint2(pack_f16(kg[0], kg[1]), pack_f16(kg[2], kg[3]));
                 SM_AT(uint2, scr + S_QG + o) = make_uint2(pack_f16(qg[0], qg[1]), pack_f16(qg[2], qg[3]));
-                SM_AT(uint2, sl + L_Z + sw128_32rows(r, c0)) = make_uint2(pack_bf16(kg[0], kg[1]), pack_bf16(kg[2], kg[3]));
-                SM_AT(uint2, sl + L_Z + sw128_32rows(16 + r, c0)) = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(r, c0)) =
+                    make_uint2(pack_bf16(kg[0] * gp[0], kg[1] * gp[1]), pack_bf16(kg[2] * gp[2], kg[3] * gp[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(16 + r, c0)) =
+                    make_uint2(pack_bf16(qg[0] * gp[0], qg[1] * gp[1]), pack_bf16(qg[2] * gp[2], qg[3] * gp[3]));
                 const uint2 vw = vwv[i];
                 SM_AT(uint2, sl + L_V16 + raw_off(r, c0)) = make_uint2(pack_f16(bf16_lo(vw.x), bf16_hi(vw.x)),
                                                                        pack_f16(bf16_lo(vw.y), bf16_hi(vw.y)));
@@ -595,189 +605,185 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 SM_AT(uint2, scr + S_KRL + o) = make_uint2(l0, l1);
             }
             named_bar_sync(bar_id, 128);
-            if (lt == 0) mbar_arrive(bar(B_RAW_EMPTY + rs));
-
-            // A (warps 0, 2) and P (warps 1, 3), each warp over one channel half;
-            // two bf16 products per entry: Kl, Ql rounded once, Kr as hi + lo
-            const bool isP = lw & 1;
-            const int khalf = lw >> 1;
-            Frag16 acc;
-            chunk_gram_x2<4>(scr + (isP ? S_QLH : S_KLH), scr + S_KRH, scr + S_KRL, acc, lane, 4 * khalf);
-            {
-                const uint32_t xa = scr + S_AX + (isP ? 1024 : 0) + lane * 16;
-                if (khalf) {
-                    SM_AT(float4, xa) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
-                    SM_AT(float4, xa + 512) = make_float4(acc.c[1][0], acc.c[1][1], acc.c[1][2], acc.c[1][3]);
-                }
-                named_bar_sync(bar_id, 128);
-                if (!khalf) {
-                    const float4 x0 = SM_AT(const float4, xa), x1 = SM_AT(const float4, xa + 512);
-                    acc.c[0][0] += x0.x; acc.c[0][1] += x0.y; acc.c[0][2] += x0.z; acc.c[0][3] += x0.w;
-                    acc.c[1][0] += x1.x; acc.c[1][1] += x1.y; acc.c[1][2] += x1.z; acc.c[1][3] += x1.w;
-                }
+            if (lt == 0) {
+                mbar_arrive(bar(B_RAW_EMPTY + rs));
+                mbar_arrive(bar(B_P2 + n % NP));  // Kbar_n and gamma_n are in the slot
             }
-            // cross-chunk products on warps 1..3 while warp 0 inverts (slots n-1, n-2)
-            const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
-            Frag16 hw;  // warp 1: H^w = Kbar_{n-1} (K*Gamma)^T;  warp 2: H^q = Kbar_{n-1} (Q*Gamma)^T
-            frag_zero(hw);
-            if (lw == 0) {
-                // A = strictly-lower, rows scaled by beta; T' = (I + A)^-1 diag(beta)
-                const float bg = SM_AT(const float, scr + S_BETA + g * 4);
-                const float bg8 = SM_AT(const float, scr + S_BETA + (g + 8) * 4);
+
+            // A (warps 0, 2) and P (warps 1, 3) partial sums over one channel half each;
+            // two bf16 products per entry: Kl, Ql rounded once, Kr as hi + lo
+            {
+                Frag16 acc;
+                chunk_gram_x2<4>(scr + ((lw & 1) ? S_QLH : S_KLH), scr + S_KRH, scr + S_KRL, acc, lane, 4 * (lw >> 1));
+                const uint32_t gp = scr + S_GP + xb * 4096 + lw * 1024 + lane * 16;
+                SM_AT(float4, gp) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
+                SM_AT(float4, gp + 512) = make_float4(acc.c[1][0], acc.c[1][1], acc.c[1][2], acc.c[1][3]);
+                mbar_arrive(bar(B_GRAM + 2 * ln + xb));
+            }
+
+            // cross-chunk products, one per warp (slots n-1, n-2; for n < 2 they read stale
+            // slots and are stored but never used):
+            //   warp 0: H^w = Kbar_{n-1} (K Gamma)^T,   warp 1: H^q = Kbar_{n-1} (Q Gamma)^T,
+            //   warps 2, 3: H'' = Kbar_{n-2} Diag(gamma_{n-1}) [K Gamma ; Q Gamma]^T, one half each
+            if (n >= 1 && !wait_bar(bar(B_P2 + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+            {
+                const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
+                const uint32_t zt = scr + ((lw & 1) ? S_QG : S_KG) + b_row;
+                const uint32_t hx = scr + S_HX + xb * 1536;
+                float hc[2][4];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
-                        acc.c[nt][i] = j < r ? acc.c[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
-                    }
-                Frag16 T;
-                unit_lower_inverse(acc, T, g, t);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 8 * nt + 2 * t;
-                    const float2 bc = SM_AT(const float2, scr + S_BETA + col * 4);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = g + 8 * hh;
-                        const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
-                        SM_AT(uint32_t, scr + S_TP + r * M_LD + col * 2) = w;
-                        SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
-                        // Phi rows 0..15: [-T', 0]
-                        SM_AT(float2, sl + L_PHI + cm32(r, col)) = make_float2(-h_lo(w), -h_hi(w));
-                        SM_AT(float2, sl + L_PHI + cm32(r, 16 + col)) = make_float2(0.f, 0.f);
-                    }
-                }
-            } else {
-                if (lw == 1) {
-                    // P = lower (diagonal included)
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = g + 8 * hh, j = 8 * nt + 2 * t;
-                            const float v0 = j <= r ? acc.c[nt][2 * hh] : 0.f;
-                            const float v1 = j + 1 <= r ? acc.c[nt][2 * hh + 1] : 0.f;
-                            SM_AT(uint32_t, scr + S_PP + r * M_LD + j * 2) = pack_f16(v0, v1);
-                        }
-                }
-                if (n >= 1 && !wait_bar(bar(B_PREP_FULL + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
-                // for n < 2 the products below read stale slots; they are stored but never used
-                if (lw < 3) {
-                    const uint32_t zt = scr + (lw == 1 ? S_KG : S_QG) + b_row;
+                for (int i = 0; i < 2; ++i) hc[i][0] = hc[i][1] = hc[i][2] = hc[i][3] = 0.f;
+                if (lw < 2) {
 #pragma unroll
                     for (int kb = 0; kb < 8; ++kb) {
                         const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));  // A rows j, k = c
                         uint32_t aK[4], bz[4];
                         ldsm_x4(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
                         ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
-                        mma_f16(hw.c[0], aK, bz[0], bz[1]);
-                        mma_f16(hw.c[1], aK, bz[2], bz[3]);
+                        mma_f16(hc[0], aK, bz[0], bz[1]);
+                        mma_f16(hc[1], aK, bz[2], bz[3]);
                     }
-                    if (lw == 1) {  // H^w as an f16 A fragment, for warp 2's half of the correction
-                        uint32_t aH[4];
-                        frag_as_a(hw, aH);
-                        SM_AT(uint4, scr + S_GX + lane * 16) = make_uint4(aH[0], aH[1], aH[2], aH[3]);
+                    if (lw == 0) {
+                        SM_AT(uint4, hx + lane * 16) = make_uint4(pack_f16(hc[0][0], hc[0][1]), pack_f16(hc[0][2], hc[0][3]),
+                                                                  pack_f16(hc[1][0], hc[1][1]), pack_f16(hc[1][2], hc[1][3]));
+                    } else {
+                        SM_AT(float4, hx + 512 + lane * 16) = make_float4(hc[0][0], hc[0][1], hc[0][2], hc[0][3]);
+                        SM_AT(float4, hx + 1024 + lane * 16) = make_float4(hc[1][0], hc[1][1], hc[1][2], hc[1][3]);
                     }
                 } else {
-                    // H'' = Kbar_{n-2} Diag(gamma_{n-1}) Z^T (16 x 32), stored as [n = column][k = j]
-                    float hp[4][4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) hp[i][0] = hp[i][1] = hp[i][2] = hp[i][3] = 0.f;
 #pragma unroll
                     for (int kb = 0; kb < 8; ++kb) {
-                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));  // A rows j, k = c
-                        uint32_t aK[4], bk[4], bq[4];
+                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));
+                        uint32_t aK[4], bz[4];
                         ldsm_x4(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
-                        ldsm_x4(scr + S_KG + b_row + 32 * kb, bk[0], bk[1], bk[2], bk[3]);
-                        ldsm_x4(scr + S_QG + b_row + 32 * kb, bq[0], bq[1], bq[2], bq[3]);
+                        ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
                         const float2 gl = SM_AT(const float2, prev + L_GAM + (16 * kb + 2 * t) * 4);
                         const float2 gh = SM_AT(const float2, prev + L_GAM + (16 * kb + 8 + 2 * t) * 4);
                         const uint32_t gk0 = pack_f16(gl.x, gl.y), gk1 = pack_f16(gh.x, gh.y);
-                        mma_f16(hp[0], aK, hmul2(bk[0], gk0), hmul2(bk[1], gk1));
-                        mma_f16(hp[1], aK, hmul2(bk[2], gk0), hmul2(bk[3], gk1));
-                        mma_f16(hp[2], aK, hmul2(bq[0], gk0), hmul2(bq[1], gk1));
-                        mma_f16(hp[3], aK, hmul2(bq[2], gk0), hmul2(bq[3], gk1));
+                        mma_f16(hc[0], aK, hmul2(bz[0], gk0), hmul2(bz[1], gk1));
+                        mma_f16(hc[1], aK, hmul2(bz[2], gk0), hmul2(bz[3], gk1));
                     }
-#pragma unroll
-                    for (int nu = 0; nu < 4; nu += 2)
-                        stsm_x4_t(sl + L_HP + nu * 256 + stsm_row, pack_f16(hp[nu][0], hp[nu][1]), pack_f16(hp[nu][2], hp[nu][3]),
-                                  pack_f16(hp[nu + 1][0], hp[nu + 1][1]), pack_f16(hp[nu + 1][2], hp[nu + 1][3]));
-                }
-            }
-            named_bar_sync(bar_id, 128);
-
-            // M = P T' (warps 0, 2). Warp 0 writes TM rows 16..31 = s M and Phi rows 16..31 =
-            // [-s M, s I]; (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q] is written by
-            // warp 1 (first 16 columns) and warp 2 (last 16)
-            if (lw == 1) {
-                uint32_t aH[4];
-                frag_as_a(hw, aH);
-                // B[k = m][n] = -T'[n][m]: the T' tile rows are n
-                uint32_t bt[4];
-                ldsm_x4(scr + S_TP + (ri + 8 * (mi >> 1)) * M_LD + 16 * (mi & 1), bt[0], bt[1], bt[2], bt[3]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) bt[i] ^= 0x80008000u;
-                float cf[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
-                mma_f16(cf[0], aH, bt[0], bt[1]);
-                mma_f16(cf[1], aH, bt[2], bt[3]);
-                stsm_x4_t(sl + L_CC + stsm_row, pack_f16(cf[0][0], cf[0][1]), pack_f16(cf[0][2], cf[0][3]),
-                          pack_f16(cf[1][0], cf[1][1]), pack_f16(cf[1][2], cf[1][3]));
-            } else if (lw != 3) {
-                uint32_t aP[4], b0, b1, b2, b3;
-                ldsm_x4(scr + S_PP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), aP[0], aP[1], aP[2], aP[3]);
-                ldsm_x4_t(scr + S_TP + (ri + 8 * (mi & 1)) * M_LD + 16 * (mi >> 1), b0, b1, b2, b3);
-                float m[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) m[i][0] = m[i][1] = m[i][2] = m[i][3] = 0.f;
-                mma_f16(m[0], aP, b0, b1);
-                mma_f16(m[1], aP, b2, b3);
-                // s M rounded to f16 once, shared by TM, Phi and the correction
-                uint32_t sm16[2][2];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) sm16[nt][hh] = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
-                if (lw == 0) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = g + 8 * hh, col = 8 * nt + 2 * t;
-                            const uint32_t w = sm16[nt][hh];
-                            SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = w;
-                            SM_AT(float2, sl + L_PHI + cm32(16 + r, col)) = make_float2(-h_lo(w), -h_hi(w));
-                            SM_AT(float2, sl + L_PHI + cm32(16 + r, 16 + col)) =
-                                make_float2(r == col ? sc : 0.f, r == col + 1 ? sc : 0.f);
-                        }
-                } else {
-                    // A operand: H^w from warp 1; B[k = m][n = i] = -s M[i][m], from the fragments of M
-                    const uint4 ah = SM_AT(const uint4, scr + S_GX + lane * 16);
-                    const uint32_t aH[4] = {ah.x, ah.y, ah.z, ah.w};
-                    float cf[2][4];
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) cf[nt][i] = 0.f;
-                    mma_f16(cf[0], aH, sm16[0][0] ^ 0x80008000u, sm16[1][0] ^ 0x80008000u);
-                    mma_f16(cf[1], aH, sm16[0][1] ^ 0x80008000u, sm16[1][1] ^ 0x80008000u);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) cf[nt][i] += sc * hw.c[nt][i];  // + s H^q (this warp's product)
-                    stsm_x4_t(sl + L_CC + 512 + stsm_row, pack_f16(cf[0][0], cf[0][1]), pack_f16(cf[0][2], cf[0][3]),
-                              pack_f16(cf[1][0], cf[1][1]), pack_f16(cf[1][2], cf[1][3]));
+                    // H''^T rows n = Z row (16 per warp), columns k = j
+                    stsm_x4_t(sl + L_HP + (lw == 2 ? 0 : 512) + stsm_row, pack_f16(hc[0][0], hc[0][1]),
+                              pack_f16(hc[0][2], hc[0][3]), pack_f16(hc[1][0], hc[1][1]), pack_f16(hc[1][2], hc[1][3]));
                 }
             }
             tc::fence_async_smem();
-            const bool stop = named_bar_or(bar_id, 128, failed);
-            if (lt == 0) {
-                mbar_arrive(bar(B_PREP_FULL + n % NP));
-                if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));
+            mbar_arrive(bar(B_HRDY + 2 * ln + xb));
+            if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));  // last read of slot n - 2
+        }
+    } else {
+        // ---------------------------------------------------------------- finishers
+        // one warp per prep lane: A and P from the lane's partial sums, T' = (I + A)^-1 diag(beta),
+        // M = P T', the TM and Phi operands and (H Phi^T)^T, then the slot is handed on.
+        const int ln = warp - 14;
+        const uint32_t scr = sb + OFF_SCR + ln * SCR;
+        const float sc = p.scale;
+        const int g = lane >> 2, t = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+        const uint32_t stsm_row = (mi >> 1) * 256 + (mi & 1) * 128 + ri * 16;
+        constexpr uint32_t NEG2 = 0x80008000u;  // negates both halves of an f16 pair
+        for (int n = ln; n < nch; n += 2) {
+            const int xb = (n >> 1) & 1;
+            const uint32_t xpar = static_cast<uint32_t>(n >> 2) & 1;
+            const uint32_t sl = slot(n);
+            const uint32_t gp = scr + S_GP + xb * 4096 + lane * 16, hx = scr + S_HX + xb * 1536;
+            const uint32_t bet = scr + S_BETA + xb * 64;
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_GRAM + 2 * ln + xb), xpar, flags))) break;
+            // A = strictly-lower part with rows scaled by beta; P = lower part (diagonal included)
+            Frag16 A, P;
+            {
+                float4 x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = SM_AT(const float4, gp + 512 * i);  // [warp][tile]
+                const float4 a0 = make_float4(x[0].x + x[4].x, x[0].y + x[4].y, x[0].z + x[4].z, x[0].w + x[4].w);
+                const float4 a1 = make_float4(x[1].x + x[5].x, x[1].y + x[5].y, x[1].z + x[5].z, x[1].w + x[5].w);
+                const float4 p0 = make_float4(x[2].x + x[6].x, x[2].y + x[6].y, x[2].z + x[6].z, x[2].w + x[6].w);
+                const float4 p1 = make_float4(x[3].x + x[7].x, x[3].y + x[7].y, x[3].z + x[7].z, x[3].w + x[7].w);
+                const float av[2][4] = {{a0.x, a0.y, a0.z, a0.w}, {a1.x, a1.y, a1.z, a1.w}};
+                const float pv[2][4] = {{p0.x, p0.y, p0.z, p0.w}, {p1.x, p1.y, p1.z, p1.w}};
+                const float bg = SM_AT(const float, bet + g * 4), bg8 = SM_AT(const float, bet + (g + 8) * 4);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = g + 8 * (i >> 1), j = 8 * nt + 2 * t + (i & 1);
+                        A.c[nt][i] = j < r ? av[nt][i] * ((i >> 1) ? bg8 : bg) : 0.f;
+                        P.c[nt][i] = j <= r ? pv[nt][i] : 0.f;
+                    }
             }
-            if (stop) break;
+            Frag16 T;
+            unit_lower_inverse(A, T, g, t);
+            // T' = T diag(beta) rounded to f16 once: tw[col block][row block] in fragment layout;
+            // TM rows 0..15 = T', Phi rows 0..15 = [-T', 0]
+            uint32_t tw[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = 8 * nt + 2 * t;
+                const float2 bc = SM_AT(const float2, bet + col * 4);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = g + 8 * hh;
+                    const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
+                    tw[nt][hh] = w;
+                    SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
+                    SM_AT(float2, sl + L_PHI + cm32(r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                    SM_AT(float2, sl + L_PHI + cm32(r, 16 + col)) = make_float2(0.f, 0.f);
+                }
+            }
+            // M = P T' (B operand: transposed 8x8 blocks of T'); s M rounded to f16 once, shared by
+            // TM rows 16..31, Phi rows 16..31 = [-s M, s I] and the correction
+            uint32_t sm16[2][2];
+            {
+                uint32_t aP[4];
+                frag_as_a(P, aP);
+                float m[2][4];
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    m[nb][0] = m[nb][1] = m[nb][2] = m[nb][3] = 0.f;
+                    mma_f16(m[nb], aP, movm_t(tw[nb][0]), movm_t(tw[nb][1]));
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = g + 8 * hh, col = 8 * nt + 2 * t;
+                        const uint32_t w = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
+                        sm16[nt][hh] = w;
+                        SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = w;
+                        SM_AT(float2, sl + L_PHI + cm32(16 + r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                        SM_AT(float2, sl + L_PHI + cm32(16 + r, 16 + col)) = make_float2(r == col ? sc : 0.f, r == col + 1 ? sc : 0.f);
+                    }
+            }
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_HRDY + 2 * ln + xb), xpar, flags))) break;
+            // (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q]: B[k = m][n] = -T'[n][m] and
+            // -s M[n][m] come straight from the fragments of T' and s M
+            {
+                const uint4 ah = SM_AT(const uint4, hx + lane * 16);
+                const uint32_t aH[4] = {ah.x, ah.y, ah.z, ah.w};
+                const float4 q0 = SM_AT(const float4, hx + 512 + lane * 16), q1 = SM_AT(const float4, hx + 1024 + lane * 16);
+                float cf[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
+                mma_f16(cf[0], aH, tw[0][0] ^ NEG2, tw[1][0] ^ NEG2);
+                mma_f16(cf[1], aH, tw[0][1] ^ NEG2, tw[1][1] ^ NEG2);
+                mma_f16(cf[2], aH, sm16[0][0] ^ NEG2, sm16[1][0] ^ NEG2);
+                mma_f16(cf[3], aH, sm16[0][1] ^ NEG2, sm16[1][1] ^ NEG2);
+                cf[2][0] = fmaf(sc, q0.x, cf[2][0]); cf[2][1] = fmaf(sc, q0.y, cf[2][1]);
+                cf[2][2] = fmaf(sc, q0.z, cf[2][2]); cf[2][3] = fmaf(sc, q0.w, cf[2][3]);
+                cf[3][0] = fmaf(sc, q1.x, cf[3][0]); cf[3][1] = fmaf(sc, q1.y, cf[3][1]);
+                cf[3][2] = fmaf(sc, q1.z, cf[3][2]); cf[3][3] = fmaf(sc, q1.w, cf[3][3]);
+#pragma unroll
+                for (int nu = 0; nu < 4; nu += 2)
+                    stsm_x4_t(sl + L_CC + nu * 256 + stsm_row, pack_f16(cf[nu][0], cf[nu][1]), pack_f16(cf[nu][2], cf[nu][3]),
+                              pack_f16(cf[nu + 1][0], cf[nu + 1][1]), pack_f16(cf[nu + 1][2], cf[nu + 1][3]));
+            }
+            tc::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_FDONE + 2 * ln + xb));
+                mbar_arrive(bar(B_PREP_FULL + n % NP));
+            }
         }
     }
 
