@@ -14,23 +14,28 @@
 // The state product is formed two chunks ahead from the decayed state two
 // chunks back and corrected by the two rank-16 updates in between (exact in
 // real arithmetic):
-//   S_n Z_n^T = Sb_{n-2} Z_n^T + E_{n-2} H''_n + E_{n-1} H_n,
-//   Sb_{n-2} = bf16(S_{n-2} Diag(gamma_{n-2} gamma_{n-1})),
+//   S_n Z_n^T = Sb_{n-2} Z'_n^T + E_{n-2} H''_n + E_{n-1} H_n,
+//   Sb_{n-2} = bf16(S_{n-2} Diag(gamma_{n-2})),  Z'_n = Z_n Diag(gamma_{n-1}),
 //   H_n = Kbar_{n-1} Z_n^T,  H''_n = Kbar_{n-2} Diag(gamma_{n-1}) Z_n^T,
 // so D_n = V_n^T TM_n^T + X_n Phi_n^T + E_{n-1} (H_n Phi_n^T), where
-// X_n = Sb_{n-2} Z_n^T + E_{n-2} H''_n is accumulated in tensor memory and
+// X_n = Sb_{n-2} Z'_n^T + E_{n-2} H''_n is accumulated in tensor memory and
 // read back as the (tf32) A operand of the Phi product. Only the last term
 // depends on the previous chunk's result, so each chunk's critical path is one
 // 16-deep MMA plus one commit, and the prep lanes never form the 32 x K rows
-// of w and q^ themselves.
+// of w and q^ themselves. The slot stores Z' (the prep of chunk n reads
+// gamma_{n-1} from the other lane's slot), so the state warps scale the state
+// by their own chunk's gate only.
 //
-// Warp roles (448 threads):
+// Warp roles (512 threads):
 //   warp 0      TMA producer (lane 0); allocates / frees tensor memory.
 //   warp 1      MMA issuer (lane 0).
 //   warps 2-5   state warps, one V row per thread (tensor-memory lane):
 //               read [E|O], hand E to the tensor core, decay the state
 //               (S <- S Diag(gamma)) and keep its bf16 copy, store outputs.
-//   warps 6-13  two prep lanes of four warps, alternate chunks.
+//   warps 6-13  two prep lanes of four warps, alternate chunks: gate, scaled
+//               key / query tiles, chunk-product partial sums, H and H''.
+//   warps 14-15 one finisher per lane: T', M, TM, Phi, (H Phi^T)^T; hands
+//               the slot to the tensor core.
 // Tensor memory (512 columns): state fp32 [0,128), D x3 [128,224),
 // E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384), X [384,416).
 //
