@@ -39,6 +39,21 @@ _lib.kda_fwd.argtypes = FWD_ARGTYPES
 _lib.kda_fwd.restype = _I
 _lib.kda_fwd_host.argtypes = FWD_ARGTYPES
 _lib.kda_fwd_host.restype = _I
+_lib.kda_fwd_flat.argtypes = FWD_ARGTYPES
+_lib.kda_fwd_flat.restype = _I
+
+
+class FwdArgs(ctypes.Structure):
+    """ctypes mirror of ``kda_fwd_args`` (include/kda.h), field for field."""
+    _fields_ = [("q", _P), ("k", _P), ("v", _P), ("g", _P), ("beta", _P), ("out", _P),
+                ("A_log", _P), ("dt_bias", _P), ("initial_state", _P), ("final_state", _P),
+                ("cu_seqlens", _P), ("initial_dtype", _I), ("final_dtype", _I),
+                ("scale", _F), ("lower_bound", _F),
+                ("N", _I64), ("B", _I64), ("T", _I64), ("H", _I64), ("K", _I64), ("V", _I64)]
+
+
+_lib.kda_fwd_packed.argtypes = [ctypes.POINTER(FwdArgs), _P]
+_lib.kda_fwd_packed.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
 _lib.kda_check_device_status.argtypes = [_P]
 _lib.kda_check_device_status.restype = _I
@@ -132,6 +147,42 @@ def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0
                           _ptr(initial_state), _state_code(initial_state),
                           _ptr(final_state), _state_code(final_state),
                           _ptr(cu_seqlens), N, B, T, H, K, V, ctypes.c_void_p(stream))
+    _raise(st)
+    return out, final_state
+
+
+def fwd_flat(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+             initial_state=None, final_state=None, cu_seqlens=None):
+    """``fwd`` through the ``kda_fwd_flat`` entry point (the same C call under its second name)."""
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=True)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_fwd_flat(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                               _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                               _ptr(initial_state), _state_code(initial_state),
+                               _ptr(final_state), _state_code(final_state),
+                               _ptr(cu_seqlens), N, B, T, H, K, V, ctypes.c_void_p(stream))
+    _raise(st)
+    return out, final_state
+
+
+def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+               initial_state=None, final_state=None, cu_seqlens=None):
+    """``fwd`` through the argument-struct entry point ``kda_fwd_packed``."""
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=True)
+    a = FwdArgs()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out), ("A_log", A_log),
+                    ("dt_bias", dt_bias), ("initial_state", initial_state), ("final_state", final_state),
+                    ("cu_seqlens", cu_seqlens)):
+        setattr(a, name, None if t is None else t.data_ptr())
+    a.initial_dtype, a.final_dtype = _state_code(initial_state), _state_code(final_state)
+    a.scale, a.lower_bound = float(scale), float(lower_bound)
+    a.N, a.B, a.T, a.H, a.K, a.V = N, B, T, H, K, V
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_fwd_packed(ctypes.byref(a), ctypes.c_void_p(stream))
     _raise(st)
     return out, final_state
 

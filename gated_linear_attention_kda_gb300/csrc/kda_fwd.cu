@@ -263,6 +263,24 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
     return KDA_OK;
 }
 
+KDA_API kda_status kda_fwd_flat(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                                const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                                kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                                int64_t H, int64_t K, int64_t V, void *stream)
+{
+    return kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype,
+                   final_state, final_dtype, cu_seqlens, N, B, T, H, K, V, stream);
+}
+
+KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream)
+{
+    if (!a) return fail(KDA_ERR_NULL, "kda_fwd_packed: NULL argument struct");
+    return kda_fwd(a->q, a->k, a->v, a->g, a->beta, a->scale, a->out, a->A_log, a->dt_bias, a->lower_bound,
+                   a->initial_state, a->initial_dtype, a->final_state, a->final_dtype, a->cu_seqlens, a->N, a->B,
+                   a->T, a->H, a->K, a->V, stream);
+}
+
 KDA_API kda_status kda_check_device_status(void *stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

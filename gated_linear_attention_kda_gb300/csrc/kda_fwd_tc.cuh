@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < NP; ++i) {
             mbar_init(bar(B_PREP_FULL + i), 1);
-            mbar_init(bar(B_PREP_EMPTY + i), 1 + 128);  // the state update's commit + the lane reading it two chunks later
+            mbar_init(bar(B_PREP_EMPTY + i), 1 + 4);  // the state update's commit + the lane's warps reading it two chunks later
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_D + i), 1);
@@ -204,9 +204,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(bar(B_F), 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(bar(B_P2 + i), 1);
-            mbar_init(bar(B_GAM + i), 32);
-            mbar_init(bar(B_GRAM + i), 128);
-            mbar_init(bar(B_HRDY + i), 128);
+            mbar_init(bar(B_GAM + i), 1);
+            mbar_init(bar(B_GRAM + i), 4);
+            mbar_init(bar(B_HRDY + i), 4);
             mbar_init(bar(B_FDONE + i), 1);
         }
         flags[0] = 0;
@@ -551,7 +551,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (rq == 3) {
                     SM_AT(float4, sl + L_GAM + c0 * 4) =
                         make_float4(ex2_approx(ge[0]), ex2_approx(ge[1]), ex2_approx(ge[2]), ex2_approx(ge[3]));
-                    mbar_arrive(bar(B_GAM + n % NP));
+                    __syncwarp();  // the warp's stores happen before its one arrival
+                    if (lane == 0) mbar_arrive(bar(B_GAM + n % NP));
                 }
             }
             // gamma_{n-1} of this thread's channels (the previous chunk, the other lane): the state
@@ -623,7 +624,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t gp = scr + S_GP + xb * 4096 + lw * 1024 + lane * 16;
                 SM_AT(float4, gp) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
                 SM_AT(float4, gp + 512) = make_float4(acc.c[1][0], acc.c[1][1], acc.c[1][2], acc.c[1][3]);
-                mbar_arrive(bar(B_GRAM + 2 * ln + xb));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_GRAM + 2 * ln + xb));
             }
 
             // cross-chunk products, one per warp (slots n-1, n-2; for n < 2 they read stale
@@ -674,8 +676,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             tc::fence_async_smem();
-            mbar_arrive(bar(B_HRDY + 2 * ln + xb));
-            if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));  // last read of slot n - 2
+            __syncwarp();  // one arrival per warp, after all its lanes' stores and reads
+            if (lane == 0) {
+                mbar_arrive(bar(B_HRDY + 2 * ln + xb));
+                if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));  // last read of slot n - 2
+            }
         }
     } else {
         // ---------------------------------------------------------------- finishers

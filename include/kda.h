@@ -119,6 +119,41 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
                            void *stream);
 
 /*
+ * kda_fwd_flat -- the same call as kda_fwd under a second name, for callers
+ * that pair it with the argument-struct form below.
+ */
+KDA_API kda_status kda_fwd_flat(const void *q, const void *k, const void *v, const void *g,
+                                const void *beta, float scale, void *out,
+                                const float *A_log, const float *dt_bias, float lower_bound,
+                                const void *initial_state, kda_dtype initial_dtype,
+                                void *final_state, kda_dtype final_dtype,
+                                const int64_t *cu_seqlens, int64_t N,
+                                int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                                void *stream);
+
+/*
+ * kda_fwd_args / kda_fwd_packed -- the same operation with its arguments in
+ * one struct. Every field has the meaning, layout and ownership of the
+ * kda_fwd argument of the same name; the struct itself is read during the
+ * call only and may be reused or freed when it returns. A NULL `a` returns
+ * KDA_ERR_NULL; every other check and error is kda_fwd's.
+ */
+typedef struct kda_fwd_args {
+    const void *q, *k, *v, *g, *beta; /* bf16 [B, T, H, 128] / beta bf16 [B, T, H] */
+    void *out;                         /* bf16 [B, T, H, 128], written */
+    const float *A_log;                /* fp32 [H] or NULL */
+    const float *dt_bias;              /* fp32 [H, 128] or NULL */
+    const void *initial_state;         /* [B|N, H, 128, 128] or NULL */
+    void *final_state;                 /* [B|N, H, 128, 128] or NULL, written */
+    const int64_t *cu_seqlens;         /* int64 [N + 1] or NULL */
+    kda_dtype initial_dtype, final_dtype;
+    float scale, lower_bound;
+    int64_t N, B, T, H, K, V;
+} kda_fwd_args;
+
+KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream);
+
+/*
  * kda_fwd_host -- the same operation on HOST buffers (same layouts and
  * arguments as kda_fwd, every pointer a host pointer; pinned memory gives
  * the fastest copies). It stages the inputs in stream-ordered device memory

@@ -25,14 +25,37 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     syms = declared_symbols()
-    assert {"kda_fwd", "kda_fwd_host", "kda_check_device_status", "kda_last_error", "kda_plan",
-            "kda_gate_scale", "kda_version"} <= set(syms)
+    assert {"kda_fwd", "kda_fwd_flat", "kda_fwd_packed", "kda_fwd_host", "kda_check_device_status",
+            "kda_last_error", "kda_plan", "kda_gate_scale", "kda_version"} <= set(syms)
 
 
 def test_library_exports_every_declared_symbol(kda):
     lib = ctypes.CDLL(kda.LIB_PATH)
     for s in declared_symbols():
         assert hasattr(lib, s), f"libkda.so does not export {s}"
+
+
+
+def test_struct_entry_layout_matches_the_header(kda, tmp_path):
+    """The ctypes mirror of kda_fwd_args has the C struct's size and field offsets
+    (a C program including the header prints them), and a NULL struct is rejected."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in kda.FwdArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"kda.h\"\nint main(void) {\n"
+                   + 'printf("%zu\\n", sizeof(kda_fwd_args));\n'
+                   + "".join(f'printf("%zu\\n", offsetof(kda_fwd_args, {f}));\n' for f in fields)
+                   + "return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(kda.FwdArgs)
+    assert got[1:] == [getattr(kda.FwdArgs, f).offset for f in fields]
+    assert kda.library().kda_fwd_packed(None, None) == 1  # KDA_ERR_NULL
 
 
 def test_gate_scale_matches_the_page_constant(kda):

@@ -152,6 +152,22 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(fin.double().numpy(), s_dev)
 
 
+
+@pytest.mark.parametrize("entry", ["fwd_flat", "fwd_packed"])
+def test_flat_and_struct_entry_points_match_kda_fwd(entry):
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", T=45)
+    o_dev, s_dev = run_gpu(d)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.full_like(c["v"], float("nan"))
+    fin = torch.full_like(c["initial_state"], float("nan"))
+    getattr(kda, entry)(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+                        d["lower_bound"], c["initial_state"], fin)
+    kda.check_device_status()
+    assert np.array_equal(out.float().cpu().double().numpy(), o_dev)
+    assert np.array_equal(fin.cpu().double().numpy(), s_dev)
+
+
 # ------------------------------------------------------------ full-size workloads
 
 def test_full_b8_t4096_h16_sampled_heads():
