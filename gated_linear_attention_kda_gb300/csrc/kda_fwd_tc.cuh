@@ -610,6 +610,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 SM_AT(uint2, scr + S_KRH + o) = make_uint2(h0, h1);
                 SM_AT(uint2, scr + S_KRL + o) = make_uint2(l0, l1);
             }
+            tc::fence_async_smem();  // Z', V and Kbar are read by the tensor core
             named_bar_sync(bar_id, 128);
             if (lt == 0) {
                 mbar_arrive(bar(B_RAW_EMPTY + rs));
@@ -673,9 +674,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // H''^T rows n = Z row (16 per warp), columns k = j
                     stsm_x4_t(sl + L_HP + (lw == 2 ? 0 : 512) + stsm_row, pack_f16(hc[0][0], hc[0][1]),
                               pack_f16(hc[0][2], hc[0][3]), pack_f16(hc[1][0], hc[1][1]), pack_f16(hc[1][2], hc[1][3]));
+                    tc::fence_async_smem();  // H''^T is read by the tensor core
                 }
             }
-            tc::fence_async_smem();
             __syncwarp();  // one arrival per warp, after all its lanes' stores and reads
             if (lane == 0) {
                 mbar_arrive(bar(B_HRDY + 2 * ln + xb));
