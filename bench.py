@@ -126,16 +126,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl"):
+    """Rank, world size and local rank from the launcher's environment; one GPU per rank
+    (``backend="gloo"`` keeps everything on the host, for tests without a GPU)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -146,14 +151,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The largest ``x`` over all ranks (every rank gets it): a job's time is its slowest rank's."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, steps, seconds):
+    """Whole-job tokens/s: every rank runs its own copy of the workload (weak scaling), so the
+    job processes ``world * tokens_per_rank`` tokens per step in the slowest rank's time."""
+    return world * tokens_per_rank * steps / seconds
 
 
 def oracle_time(d, nthreads, batch_rows):
@@ -278,7 +290,7 @@ def run_ours(args, world, rank, local):
         return
     tokens = B * T
     ms_per_step = elapsed_ms / args.steps
-    value = world * tokens * args.steps / (elapsed_ms / 1e3)
+    value = job_throughput(world, tokens, args.steps, elapsed_ms / 1e3)
     nbytes, nflops = algorithmic(WORKLOAD, d)
     hbm, tflops, src = peaks()
     achieved = nbytes / (ms_per_step / 1e3) / 1e9
@@ -302,7 +314,7 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic, "peak_source": src, "algorithmic_bytes_per_launch": nbytes,
                      "tensor_frac": (nflops / (ms_per_step / 1e3) / 1e12) / tflops},
         "cpu_baseline": cpu_baseline(d) if world == 1 or rank == 0 else None,
-        "e2e": {"value": world * tokens * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, tokens, e2e_steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks,
         "gpu_launches": args.steps,
