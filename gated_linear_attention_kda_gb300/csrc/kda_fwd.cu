@@ -42,6 +42,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -215,6 +216,13 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
         return fail(KDA_ERR_ALIGN, "state buffers must be 16-byte aligned");
     if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)) || (cu_seqlens && !aligned(cu_seqlens, 8)))
         return fail(KDA_ERR_ALIGN, "A_log, dt_bias and cu_seqlens must be naturally aligned");
+    // KDA_V_SPLIT (1, 2, 4 or 8) overrides the planned split of each state's V rows, for tuning and tests
+    int force_vs = 0;
+    if (const char *env = std::getenv("KDA_V_SPLIT")) {
+        force_vs = std::atoi(env);
+        if (force_vs != 1 && force_vs != 2 && force_vs != 4 && force_vs != 8)
+            return fail(KDA_ERR_RANGE, "KDA_V_SPLIT must be 1, 2, 4 or 8 (got '%s')", env);
+    }
 
     CUtensorMap mq, mk, mv, mg, mo;
     std::memset(&mo, 0, sizeof mo);
@@ -251,6 +259,10 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
     int vs;
     int64_t grid;
     plan(nseq * H, nsm, &vs, &grid);
+    if (force_vs) {
+        vs = force_vs;
+        grid = nseq * H * vs;
+    }
     p.vsplit = vs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (vs) {

@@ -108,6 +108,9 @@ typedef enum kda_dtype {
  * A state absent from the call is zero (initial) or not written (final).
  * Returns KDA_OK once the work is enqueued. Argument errors are detected on
  * the host before anything is launched and leave every buffer untouched.
+ * The environment variable KDA_V_SPLIT (1, 2, 4 or 8), when set, overrides the
+ * planned split of each state's V rows across CTAs (kda_plan); any other value
+ * is KDA_ERR_RANGE. Results do not depend on the split beyond rounding order.
  */
 KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, float scale, void *out,

@@ -106,6 +106,13 @@ def test_host_validation_rejects(kda, over, code):
     assert kda.library().kda_last_error()
 
 
+
+@pytest.mark.parametrize("value", ["3", "0", "16", "x"])
+def test_v_split_override_rejects_bad_values(kda, monkeypatch, value):
+    monkeypatch.setenv("KDA_V_SPLIT", value)
+    assert _call(kda) == 4  # KDA_ERR_RANGE, before anything touches a GPU
+    assert b"KDA_V_SPLIT" in kda.library().kda_last_error()
+
 def test_python_wrapper_rejects_bad_tensors(kda):
     import torch
     q = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16)

@@ -168,6 +168,39 @@ def test_flat_and_struct_entry_points_match_kda_fwd(entry):
     assert np.array_equal(fin.cpu().double().numpy(), s_dev)
 
 
+
+@pytest.mark.parametrize("vs", [1, 2, 4, 8])
+def test_forced_v_split_matches_oracle(vs, monkeypatch):
+    """Every split of the V rows (1: the tcgen05 kernel; 2, 4, 8: the warp-MMA kernel) on the same
+    ragged inputs, against the oracle."""
+    monkeypatch.setenv("KDA_V_SPLIT", str(vs))
+    _check(W.make("b2_t128_h8", T=45))
+
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_no_writes_outside_out_and_final_state(H):
+    """Canaries on both sides of out and final_state survive the call (varlen, ragged lengths)."""
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("varlen_n16_h32", lengths=[5, 16, 33], H=H)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    pad = 64
+
+    def padded(like):
+        n = like.numel()
+        big = torch.empty(n + 2 * pad, dtype=like.dtype, device="cuda")
+        big.view(torch.int16 if like.element_size() == 2 else torch.int32).fill_(0x5A5A)
+        return big, big[pad:pad + n].view(like.shape)
+
+    obig, out = padded(c["v"])
+    fbig, fin = padded(c["initial_state"])
+    before_o, before_f = obig.clone(), fbig.clone()
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+    kda.check_device_status()
+    for big, ref in ((obig, before_o), (fbig, before_f)):
+        assert torch.equal(big[:pad], ref[:pad]) and torch.equal(big[-pad:], ref[-pad:])
+
+
 # ------------------------------------------------------------ full-size workloads
 
 def test_full_b8_t4096_h16_sampled_heads():
