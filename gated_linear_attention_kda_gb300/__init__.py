@@ -54,6 +54,8 @@ class FwdArgs(ctypes.Structure):
 
 _lib.kda_fwd_packed.argtypes = [ctypes.POINTER(FwdArgs), _P]
 _lib.kda_fwd_packed.restype = _I
+_lib.kda_probe_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P]
+_lib.kda_probe_chunk.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
 _lib.kda_check_device_status.argtypes = [_P]
 _lib.kda_check_device_status.restype = _I
@@ -186,6 +188,27 @@ def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bou
     _raise(st)
     return out, final_state
 
+
+
+def probe_chunk(q, k, g, beta, A_log=None, dt_bias=None, lower_bound=-5.0, rows=16):
+    """Test hook: one chunk of one head (``q, k, g`` bf16 [16, 128], ``beta`` bf16 [16] logits,
+    ``A_log`` fp32 [1] or None, ``dt_bias`` fp32 [128] or None, all on the GPU) through the
+    per-chunk steps. Returns fp32 ``G2`` [16, 128] (log2 units, cumsum), ``beta`` [16] and
+    ``A``, ``P``, ``T`` [16, 16]."""
+    for name, t, dt, shp in (("q", q, torch.bfloat16, (16, 128)), ("k", k, torch.bfloat16, (16, 128)),
+                             ("g", g, torch.bfloat16, (16, 128)), ("beta", beta, torch.bfloat16, (16,))):
+        _check(name, t, dt, shp, True)
+    _check("A_log", A_log, torch.float32, (1,), True)
+    _check("dt_bias", dt_bias, torch.float32, (128,), True)
+    o = {n: torch.empty(shp, dtype=torch.float32, device=q.device)
+         for n, shp in (("G2", (16, 128)), ("beta", (16,)), ("A", (16, 16)), ("P", (16, 16)), ("T", (16, 16)))}
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_probe_chunk(_ptr(q), _ptr(k), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                                  float(lower_bound), int(rows), _ptr(o["G2"]), _ptr(o["beta"]), _ptr(o["A"]),
+                                  _ptr(o["P"]), _ptr(o["T"]), ctypes.c_void_p(stream))
+    _raise(st)
+    return o
 
 def fwd_host(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
              initial_state=None, final_state=None, cu_seqlens=None, device=None):

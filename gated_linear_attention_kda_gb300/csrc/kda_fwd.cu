@@ -57,6 +57,7 @@
 #include "kda_common.cuh"
 #include "kda_fwd_mma.cuh"
 #include "kda_fwd_tc.cuh"
+#include "kda_probe.cuh"
 
 namespace kda {
 
@@ -291,6 +292,26 @@ KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream)
     return kda_fwd(a->q, a->k, a->v, a->g, a->beta, a->scale, a->out, a->A_log, a->dt_bias, a->lower_bound,
                    a->initial_state, a->initial_dtype, a->final_state, a->final_dtype, a->cu_seqlens, a->N, a->B,
                    a->T, a->H, a->K, a->V, stream);
+}
+
+KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, const void *beta, const float *A_log,
+                                   const float *dt_bias, float lower_bound, int rows, float *G2, float *beta_act,
+                                   float *A, float *P, float *T, void *stream)
+{
+    t_last_error.clear();
+    if (!q || !k || !g || !beta || !G2 || !beta_act || !A || !P || !T)
+        return fail(KDA_ERR_NULL, "kda_probe_chunk: q, k, g, beta and every output are required");
+    if (rows < 1 || rows > CHUNK) return fail(KDA_ERR_SHAPE, "kda_probe_chunk: rows must lie in 1..16 (got %d)", rows);
+    if (!std::isfinite(lower_bound) || lower_bound < -5.f || lower_bound > 0.f)
+        return fail(KDA_ERR_RANGE, "lower_bound must lie in [-5, 0] (got %g)", (double)lower_bound);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    probe::kda_probe_chunk_kernel<<<1, 128, 0, s>>>(
+        static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(g),
+        static_cast<const uint16_t *>(beta), A_log, dt_bias, 0.5f * kda_gate_scale(lower_bound), rows, G2, beta_act, A,
+        P, T);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "probe launch failed: %s", cudaGetErrorString(e));
+    return KDA_OK;
 }
 
 KDA_API kda_status kda_check_device_status(void *stream)

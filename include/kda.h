@@ -174,6 +174,26 @@ KDA_API kda_status kda_fwd_host(const void *q, const void *k, const void *v, con
                                 int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
                                 void *stream);
 
+/*
+ * kda_probe_chunk -- test hook: one 16-token chunk of one head through the
+ * forward pass's per-chunk steps, built from the same device code as the
+ * kernels, so that each step can be checked on its own.
+ *   q, k, g      one chunk, bf16 [16][128] row-major (DEVICE); rows >= `rows`
+ *                are padding (k = 0, beta = 0, no gate).
+ *   beta         bf16 [16] logits (DEVICE).
+ *   A_log        one fp32 (DEVICE) or NULL; dt_bias fp32 [128] (DEVICE) or NULL.
+ *   lower_bound  in [-5, 0]; rows in 1..16.
+ * Outputs (DEVICE fp32, written): G2 [16][128] gate in log2 units with its
+ * inclusive in-chunk cumsum [LB "Conversion to the Gate Scale Factor"];
+ * beta_act [16]; A [16][16] = beta_r sum_c k_r k_j 2^{G2_r - G2_j} for j < r
+ * (else 0); P [16][16] = sum_c q_r k_j 2^{G2_r - G2_j} for j <= r (else 0);
+ * T [16][16] = (I + A)^-1 [CHUNK "Efficient 16x16 Matrix Inversion"].
+ * Asynchronous on `stream`; KDA_ERR_NULL / _SHAPE / _RANGE / _LAUNCH as kda_fwd.
+ */
+KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, const void *beta,
+                                   const float *A_log, const float *dt_bias, float lower_bound, int rows,
+                                   float *G2, float *beta_act, float *A, float *P, float *T, void *stream);
+
 /* gate_scale = lower_bound * log2(e), rounded to float, exactly as the kernel
  * receives it [LB "Conversion to the Gate Scale Factor"]. Host only. */
 KDA_API float kda_gate_scale(float lower_bound);

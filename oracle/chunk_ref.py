@@ -28,6 +28,35 @@ def _sigmoid(x):
     return 1.0 / (1.0 + np.exp(-x))
 
 
+def _chunk_matrices(qc, kc, Gam, bc):
+    """A[r, j] = beta_r sum_c k_r k_j Gamma_r / Gamma_j for j < r and P[r, j] = sum_c q_r k_j
+    Gamma_r / Gamma_j for j <= r (zero elsewhere), for one chunk's rows."""
+    L = kc.shape[0]
+    A = np.zeros((L, L))
+    P = np.zeros((L, L))
+    for r in range(L):
+        for j in range(r + 1):
+            ratio = Gam[r] / Gam[j]
+            if j < r:
+                A[r, j] = bc[r] * np.dot(kc[r] * kc[j], ratio)
+            P[r, j] = np.dot(qc[r] * kc[j], ratio)
+    return A, P
+
+
+def chunk_terms(q, k, g, beta_logit, A_log=None, dt_bias=None, lower_bound=-5.0):
+    """The per-chunk quantities of one chunk of one head, for step-by-step checks (rows
+    r = 0..L-1, inputs float64 widened from bf16: q, k, g [L, K], beta_logit [L], A_log a
+    scalar or None, dt_bias [K] or None). Returns the gate's inclusive in-chunk cumsum in
+    log2 units [L, K], beta [L], A and P as in the chunked form, and T = (I + A)^-1."""
+    a = 1.0 if A_log is None else np.exp(float(A_log))
+    b = 0.0 if dt_bias is None else np.asarray(dt_bias, np.float64)
+    G = np.cumsum(lower_bound * _sigmoid(a * (g + b)), axis=0)   # natural-log gate, summed
+    beta = _sigmoid(beta_logit)
+    A, P = _chunk_matrices(q, k, np.exp(G), beta)
+    T = np.linalg.inv(np.eye(k.shape[0]) + A)
+    return G / np.log(2.0), beta, A, P, T
+
+
 def chunk_unit(q, k, v, alpha, beta, scale, S0, chunk):
     """One (sequence, head) unit. ``q, k, alpha``: [L_tot, K]; ``v``: [L_tot, V];
     ``beta``: [L_tot] activated; ``S0``: [V, K]. Returns (out [L_tot, V], S)."""
@@ -39,15 +68,7 @@ def chunk_unit(q, k, v, alpha, beta, scale, S0, chunk):
         L = e - s
         Gam = np.cumprod(alpha[s:e], axis=0)          # [L, K]
         kc, qc, vc, bc = k[s:e], q[s:e], v[s:e], beta[s:e]
-        # ratio[r, j, c] = Gamma_r[c] / Gamma_j[c]; only j <= r is used.
-        A = np.zeros((L, L))
-        P = np.zeros((L, L))
-        for r in range(L):
-            for j in range(r + 1):
-                ratio = Gam[r] / Gam[j]
-                if j < r:
-                    A[r, j] = bc[r] * np.dot(kc[r] * kc[j], ratio)
-                P[r, j] = np.dot(qc[r] * kc[j], ratio)
+        A, P = _chunk_matrices(qc, kc, Gam, bc)
         rhs = bc[:, None] * (vc - (kc * Gam) @ S.T)   # [L, V]
         E = np.zeros_like(rhs)
         for r in range(L):                             # forward substitution

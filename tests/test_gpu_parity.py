@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path against the fp64 oracle on the same seeded
 inputs, element by element, with the stated tolerance (relative L2 <= 5e-3,
 |err| <= 2e-2 + 2e-2 |ref|) on ``out`` and ``final_state``."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -218,3 +220,41 @@ def test_full_varlen_n16_h32_sampled_heads():
 def test_full_long_context_sampled_head():
     d = W.make("b1_t131072_h32")
     _check(d, heads=[5])
+
+
+# ------------------------------------------------------------ per-step parity (one chunk)
+
+@pytest.mark.parametrize("name,b,h,chunk,rows", [
+    ("b1_t64_h1", 0, 0, 0, 16), ("b1_t64_h1", 0, 0, 1, 16), ("b1_t64_h1", 0, 0, 3, 16), ("b1_t64_h1", 0, 0, 2, 5),
+    ("b2_t128_h8", 0, 0, 0, 16), ("b2_t128_h8", 1, 5, 7, 16), ("b2_t128_h8", 0, 3, 4, 11),
+])
+def test_chunk_steps_match_the_fp64_chunk_terms(name, b, h, chunk, rows):
+    """Gate cumsum (log2), beta, A, P and T = (I + A)^-1 of one chunk, through the kernels' own
+    per-chunk device code (kda_probe_chunk), against oracle.chunk_ref.chunk_terms in fp64.
+    G2 and beta may differ by the tanh.approx sigmoid: |d sigma| <= 2.5e-4 per token, so
+    |d G2_r| <= (r + 1) |lower_bound| log2(e) 2.5e-4; A, P, T use the parity tolerance."""
+    import oracle
+    import oracle.chunk_ref as chunk_ref
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make(name)
+    sl = slice(16 * chunk, 16 * chunk + 16)
+    tiles = {x: d[x][b, sl, h].contiguous() for x in ("q", "k", "g")}
+    bt = d["beta"][b, sl, h].contiguous()
+    A_log = None if d["A_log"] is None else d["A_log"][h:h + 1].contiguous()
+    dt = None if d["dt_bias"] is None else d["dt_bias"][h].contiguous()
+    lb = d["lower_bound"]
+    o = kda.probe_chunk(tiles["q"].cuda(), tiles["k"].cuda(), tiles["g"].cuda(), bt.cuda(),
+                        None if A_log is None else A_log.cuda(), None if dt is None else dt.cuda(), lb, rows)
+    torch.cuda.synchronize()
+    f64 = lambda t: oracle.bf16_bits_to_f64(W.bf16_bits(t))
+    L = rows
+    G2, beta, A, P, T = chunk_ref.chunk_terms(f64(tiles["q"])[:L], f64(tiles["k"])[:L], f64(tiles["g"])[:L],
+                                              f64(bt)[:L], None if A_log is None else float(A_log[0]),
+                                              None if dt is None else dt.double().numpy(), lb)
+    got = {n: t.cpu().double().numpy() for n, t in o.items()}
+    bound = (np.arange(L)[:, None] + 1) * abs(lb) * math.log2(math.e) * 2.5e-4 + 1e-5
+    assert np.all(np.abs(got["G2"][:L] - G2) <= bound)
+    assert np.all(np.abs(got["beta"][:L] - beta) <= 2.5e-4 + 1e-6)
+    assert np.all(got["beta"][L:] == 0.0)
+    for n, ref in (("A", A), ("P", P), ("T", T)):
+        assert_close(n, got[n][:L, :L], ref)

@@ -277,3 +277,26 @@ def test_scale_is_linear_on_output_only():
     o2, s2 = oracle.fwd(bits["q"], bits["k"], bits["v"], bits["g"], bits["beta"], 0.25, A, db, -2.0, init)
     np.testing.assert_allclose(o2, 0.25 * o1, rtol=1e-15, atol=0)
     assert np.array_equal(s1, s2)
+
+
+# ------------------------------------------------------------ per-chunk terms (step checks)
+
+def test_chunk_terms_against_the_gate_and_closed_forms():
+    """chunk_terms: its gate cumsum is the cumsum of the oracle's gate (log2 units), T inverts
+    I + A, and with lower_bound = 0 (no decay) A and P reduce to beta-scaled and plain dot
+    products (the decay-free chunk matrices)."""
+    d = W.make("b1_t64_h1")
+    sl = slice(16, 32)
+    qb, kb, gb = (W.bf16_bits(d[x][0, sl, 0].contiguous()) for x in ("q", "k", "g"))
+    bl = _f64(W.bf16_bits(d["beta"][0, sl, 0].contiguous()))
+    A_log, dt = float(d["A_log"][0]), d["dt_bias"][0].double().numpy()
+    q, k, g = _f64(qb), _f64(kb), _f64(gb)
+    G2, beta, A, P, T = chunk_ref.chunk_terms(q, k, g, bl, A_log, dt, -5.0)
+    ga = oracle.gate(gb[:, None, :], d["A_log"][:1].numpy(), d["dt_bias"][:1].numpy(), -5.0)[:, 0, :]
+    assert np.allclose(G2, np.cumsum(ga, axis=0) / math.log(2.0), rtol=0, atol=1e-12)
+    assert np.allclose(T @ (np.eye(16) + A), np.eye(16), rtol=0, atol=1e-12)
+    assert np.allclose(beta, 1.0 / (1.0 + np.exp(-bl)))
+    G2z, _, Az, Pz, _ = chunk_ref.chunk_terms(q, k, g, bl, A_log, dt, 0.0)
+    assert np.all(G2z == 0.0)
+    assert np.allclose(Az, np.tril(beta[:, None] * (k @ k.T), -1), rtol=0, atol=1e-13)
+    assert np.allclose(Pz, np.tril(q @ k.T), rtol=0, atol=1e-13)
