@@ -74,6 +74,19 @@ def test_lower_bound_range(lb, H):
     _check(W.make("b2_t128_h8", B=1, H=H, T=70), lower_bound=lb, heads=None if H < 8 else [1, 50])
 
 
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_saturated_gates_and_betas_and_larger_values(H):
+    """Gate and beta logits pushed into saturation (|logit| up to 30: decay exp(lower_bound) or none,
+    beta 0 or 1, where the tanh form of the sigmoid is at its limits) and values 20 times larger."""
+    d = W.make("b2_t128_h8", B=1, H=H, T=70)
+    gen = torch.Generator().manual_seed(7)
+    sat = lambda t: torch.where(torch.rand(t.shape, generator=gen) < 0.5, t.float() * 30.0, t.float()).to(torch.bfloat16)
+    d["g"] = sat(d["g"])
+    d["beta"] = sat(d["beta"])
+    d["v"] = (d["v"].float() * 20.0).to(torch.bfloat16)
+    _check(d, heads=None if H < 8 else [0, 41, 79])
+
 @pytest.mark.parametrize("H", KERNEL_HEADS)
 def test_no_gate_parameters_bf16_states(H):
     d = W.make("b8_t4096_h16", B=1, T=200, H=H)
