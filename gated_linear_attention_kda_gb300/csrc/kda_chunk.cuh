@@ -120,44 +120,10 @@ __device__ __forceinline__ void split_bf16_trunc(float x0, float x1, uint32_t &h
     lo = pack_bf16(x0 - __uint_as_float(b0 & 0xffff0000u), x1 - __uint_as_float(b1 & 0xffff0000u));
 }
 
-// acc[nt] (16 rows r x 16 cols j) = sum_c X[r][c] R[j][c] over the channels
-// c in [16 kbase, 16 (kbase + NK)), from bf16 hi/lo tiles stored row-major
-// [16][136] (272-byte rows): three bf16 products Xh Rh + Xh Rl + Xl Rh give
-// ~16-bit operand precision with a bf16 exponent range.
-template <int NK>
-__device__ __forceinline__ void chunk_gram_x3(uint32_t xh, uint32_t xl, uint32_t rh, uint32_t rl, Frag16 &acc,
-                                              int lane, int kbase)
-{
-    const int mi = lane >> 3, ri = lane & 7;
-    // A operand: rows r = ri + 8 (mi & 1), cols 16 kk + 8 (mi >> 1)
-    const uint32_t aoff = (ri + 8 * (mi & 1)) * 272 + 16 * (mi >> 1) + 32 * kbase;
-    // B operand (rows j, K = c contiguous): n-tile = mi >> 1, k half = mi & 1
-    const uint32_t boff = (ri + 8 * (mi >> 1)) * 272 + 16 * (mi & 1) + 32 * kbase;
-    Frag16 cross;
-    frag_zero(acc);
-    frag_zero(cross);
-#pragma unroll
-    for (int kk = 0; kk < NK; ++kk) {
-        uint32_t ah[4], al[4], bh[4], bl[4];
-        ldsm_x4(xh + aoff + 32 * kk, ah[0], ah[1], ah[2], ah[3]);
-        ldsm_x4(xl + aoff + 32 * kk, al[0], al[1], al[2], al[3]);
-        ldsm_x4(rh + boff + 32 * kk, bh[0], bh[1], bh[2], bh[3]);
-        ldsm_x4(rl + boff + 32 * kk, bl[0], bl[1], bl[2], bl[3]);
-        mma_bf16(acc.c[0], ah, bh[0], bh[1]);
-        mma_bf16(acc.c[1], ah, bh[2], bh[3]);
-        mma_bf16(cross.c[0], ah, bl[0], bl[1]);
-        mma_bf16(cross.c[1], ah, bl[2], bl[3]);
-        mma_bf16(cross.c[0], al, bh[0], bh[1]);
-        mma_bf16(cross.c[1], al, bh[2], bh[3]);
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc.c[nt][i] += cross.c[nt][i];
-}
-
-// As chunk_gram_x3, with X rounded to bf16 once and R as hi + lo: two bf16 products
-// X Rh + X Rl per entry (R keeps ~16-bit precision, X 8 bits).
+// acc[nt] (16 rows r x 16 cols j) = sum_c X[r][c] R[j][c] over the channels c in
+// [16 kbase, 16 (kbase + NK)), from 16-bit tiles stored row-major [16][136] (272-byte rows):
+// X rounded to bf16 once and R as bf16 hi + lo, two bf16 products X Rh + X Rl per entry
+// (R keeps ~16-bit precision, X 8 bits; the bf16 exponent range holds 2^{+-58}).
 template <int NK>
 __device__ __forceinline__ void chunk_gram_x2(uint32_t x, uint32_t rh, uint32_t rl, Frag16 &acc, int lane, int kbase)
 {

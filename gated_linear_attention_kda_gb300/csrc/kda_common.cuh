@@ -102,7 +102,6 @@ __device__ __forceinline__ uint32_t raw_off(int r, int c)
 }
 
 __device__ __forceinline__ uint16_t f2bf_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-__device__ __forceinline__ uint16_t f2h_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 
 
 }  // namespace kda

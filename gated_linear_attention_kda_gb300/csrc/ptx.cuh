@@ -159,70 +159,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// ---------------------------------------------------------------- shared memory access
-__device__ __forceinline__ uint32_t lds32(uint32_t a)
-{
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint16_t lds16(uint32_t a)
-{
-    uint16_t v;
-    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float ldsf(uint32_t a)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float4 ldsf4(uint32_t a)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float2 ldsf2(uint32_t a)
-{
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v)
-{
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-
-__device__ __forceinline__ void sts16(uint32_t a, uint16_t v)
-{
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ void stsf(uint32_t a, float v)
-{
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void stsf2(uint32_t a, float x, float y)
-{
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
-}
-
 // ldmatrix is volatile (kept in order with the barrier and mbarrier asm, which
 // carry the memory clobbers) but does not fence ordinary shared-memory accesses.
 __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)

@@ -90,25 +90,6 @@ __device__ __forceinline__ void mma_ts_tf32(uint32_t d, uint32_t a_tmem, uint64_
                  : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32 (fp32 words, truncated to tf32)
-__device__ __forceinline__ void mma_ss_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                 "l"(a), "l"(b), "r"(id), "r"(accumulate)
-                 : "memory");
-}
-
-// 16 lanes x 16 columns in the m16n8 accumulator fragment layout: r[4 h + j] is
-// (lane base + lane / 4 + 8 (j >> 1), column 8 h + 2 (lane % 4) + (j & 1))
-__device__ __forceinline__ void ld16x256b_x2(uint32_t taddr, uint32_t (&r)[8])
-{
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
-}
-
 // 32 lanes (this warp's quarter) x 32 consecutive 32-bit columns
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
 {
@@ -147,17 +128,6 @@ __device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// wait::ld that also ties the loaded registers, so no use of them can be scheduled before it
-__device__ __forceinline__ void wait_ld_regs(uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
-                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-}
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace tc
