@@ -339,6 +339,52 @@ def run_launches(n):
     print(f"ran {n} launches of {WORKLOAD}")
 
 
+DECODE_B, DECODE_H = 128, 16   # 2048 fp32 states of 64 KiB: 134 MB, larger than L2
+
+
+def run_decode(args):
+    """Single-token steps (kda_decode) on DECODE_B sequences x DECODE_H heads with fp32 states
+    updated in place: one JSON line with tokens/s and the HBM fraction of the step's bytes."""
+    import torch
+
+    import gated_linear_attention_kda_gb300 as kda
+    import workloads as W
+    torch.cuda.set_device(0)
+    d = W.make("b2_t128_h8", B=DECODE_B, T=1, H=DECODE_H)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    state = c["initial_state"].clone()
+
+    def step():
+        kda.decode(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, state, c["A_log"], c["dt_bias"],
+                   d["lower_bound"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    kda.check_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    units = DECODE_B * DECODE_H
+    nbytes = units * (2 * 128 * 128 * 4 + 5 * 128 * 2 + 2) + DECODE_H * (4 + 128 * 4)
+    hbm, _, src = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "KDA decode tokens/s (one token per state, fp32 state in place)", "value": DECODE_B / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "fp32", "data": "synthetic",
+        "config": {"workload": f"decode_b{DECODE_B}_h{DECODE_H}", "B": DECODE_B, "H": DECODE_H, "K": 128, "V": 128,
+                   "l2": "states larger than L2 (134 MB), no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_source": src, "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -347,9 +393,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--launches", type=int, default=0,
                     help="profiling mode: run this many forward passes of the workload and exit (no timing)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time single-token steps (kda_decode) instead and print their own JSON line")
     args = ap.parse_args()
     if args.launches:
         run_launches(args.launches)
+        return
+    if args.decode:
+        run_decode(args)
         return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

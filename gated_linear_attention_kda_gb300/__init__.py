@@ -54,6 +54,8 @@ class FwdArgs(ctypes.Structure):
 
 _lib.kda_fwd_packed.argtypes = [ctypes.POINTER(FwdArgs), _P]
 _lib.kda_fwd_packed.restype = _I
+_lib.kda_decode.argtypes = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _I64, _I64, _I64, _I64, _P]
+_lib.kda_decode.restype = _I
 _lib.kda_probe_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P]
 _lib.kda_probe_chunk.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
@@ -189,6 +191,32 @@ def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bou
     return out, final_state
 
 
+
+
+def decode(q, k, v, g, beta, scale, out, state, A_log=None, dt_bias=None, lower_bound=-5.0):
+    """One token per (sequence, head) on the current CUDA stream, ``state`` updated in place:
+    ``q, k, v, g, out`` bf16 ``[S, H, 128]`` (or ``[S, 1, H, 128]``), ``beta`` bf16 ``[S, H]``
+    (or ``[S, 1, H]``), ``state`` bf16/fp32 ``[S, H, 128, 128]`` (kda_fwd's final_state).
+    Returns ``(out, state)``."""
+    if not isinstance(q, torch.Tensor) or q.dim() not in (3, 4):
+        raise ValueError("q must be [S, H, 128] or [S, 1, H, 128]")
+    if q.dim() == 4 and q.shape[1] != 1:
+        raise ValueError("decode takes one token per sequence (T = 1)")
+    S, H, K = q.shape[0], q.shape[-2], q.shape[-1]
+    V = v.shape[-1]
+    for name, t, shp in (("q", q, q.shape), ("k", k, q.shape), ("g", g, q.shape), ("v", v, q.shape[:-1] + (V,)),
+                         ("out", out, q.shape[:-1] + (V,)), ("beta", beta, q.shape[:-1])):
+        _check(name, t, torch.bfloat16, shp, True)
+    _check("A_log", A_log, torch.float32, (H,), True)
+    _check("dt_bias", dt_bias, torch.float32, (H, K), True)
+    _check("state", state, None, (S, H, V, K), True)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                             _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(state), _state_code(state),
+                             S, H, K, V, ctypes.c_void_p(stream))
+    _raise(st)
+    return out, state
 
 def probe_chunk(q, k, g, beta, A_log=None, dt_bias=None, lower_bound=-5.0, rows=16):
     """Test hook: one chunk of one head (``q, k, g`` bf16 [16, 128], ``beta`` bf16 [16] logits,

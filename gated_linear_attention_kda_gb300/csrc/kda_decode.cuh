@@ -1,0 +1,106 @@
+// kda_decode.cuh -- one token of KDA per (sequence, head) against a state kept in
+// place: the recurrent step next to the chunked forward pass ("FlashKDA Input
+// Tensor Shapes and DTypes ..." -- "Initial and Final States": the state carried
+// from one call to the next).
+//   a[c] = lower_bound sigmoid(exp(A_log[h]) (g[c] + dt_bias[h, c])),  beta = sigmoid(logit)
+//   S <- S Diag(exp(a)),  p = S k,  S <- S + beta (v - p) k^T,  o = scale S q
+// Bandwidth-bound (the state is read and written once per token): one CTA per (sequence,
+// head, quarter of the V rows), each warp streams eight rows, a row's 128 channels are
+// spread over the 32 lanes (four each, one 16-byte access) and its two dot products are
+// warp reductions. All arithmetic in fp32; a bf16 state is widened on load and rounded
+// to nearest on store.
+#pragma once
+#include "kda_common.cuh"
+
+namespace kda {
+namespace dec {
+
+constexpr int ROWS_PER_CTA = 32;   // V rows of one state handled by one CTA
+constexpr int THREADS = 128;       // 4 warps x 8 rows
+
+struct DecodeParams {
+    const uint16_t *q, *k, *v, *g, *beta;  // bf16 [S, H, 128] ([S, H] for beta)
+    uint16_t *out;                          // bf16 [S, H, 128]
+    const float *A_log, *dt_bias;           // [H], [H, 128] or NULL
+    void *state;                            // [S, H, 128 (V), 128 (K)], fp32 or bf16, in place
+    int state_dtype;
+    int H;
+    float scale, lower_bound;
+};
+
+__device__ __forceinline__ float bf16_to_f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+__global__ void __launch_bounds__(THREADS) kda_decode_kernel(const DecodeParams p)
+{
+    const int unit = blockIdx.x / (DH / ROWS_PER_CTA);  // (sequence, head)
+    const int quarter = blockIdx.x % (DH / ROWS_PER_CTA);
+    const int h = unit % p.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t tok = static_cast<size_t>(unit) * DH;  // [S, H, 128] offset of this (sequence, head)
+    const int c0 = 4 * lane;
+    // this lane's four channels: decay, key, query
+    const float ea = p.A_log ? expf(p.A_log[h]) : 1.f;
+    float alpha[4], kk[4], qq[4];
+    {
+        const uint2 gw = *reinterpret_cast<const uint2 *>(p.g + tok + c0);
+        const uint2 kw = *reinterpret_cast<const uint2 *>(p.k + tok + c0);
+        const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + tok + c0);
+        const uint16_t gs[4] = {static_cast<uint16_t>(gw.x), static_cast<uint16_t>(gw.x >> 16),
+                                static_cast<uint16_t>(gw.y), static_cast<uint16_t>(gw.y >> 16)};
+        const uint16_t ks[4] = {static_cast<uint16_t>(kw.x), static_cast<uint16_t>(kw.x >> 16),
+                                static_cast<uint16_t>(kw.y), static_cast<uint16_t>(kw.y >> 16)};
+        const uint16_t qs[4] = {static_cast<uint16_t>(qw.x), static_cast<uint16_t>(qw.x >> 16),
+                                static_cast<uint16_t>(qw.y), static_cast<uint16_t>(qw.y >> 16)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float b = p.dt_bias ? p.dt_bias[static_cast<size_t>(h) * DH + c0 + j] : 0.f;
+            alpha[j] = expf(p.lower_bound * sigmoid_f(ea * (bf16_to_f(gs[j]) + b)));
+            kk[j] = bf16_to_f(ks[j]);
+            qq[j] = bf16_to_f(qs[j]);
+        }
+    }
+    const float beta = sigmoid_f(bf16_to_f(p.beta[unit]));
+    const int row0 = quarter * ROWS_PER_CTA + warp * (ROWS_PER_CTA / 4);
+#pragma unroll 2
+    for (int i = 0; i < ROWS_PER_CTA / 4; ++i) {
+        const int vr = row0 + i;
+        const size_t so = (static_cast<size_t>(unit) * DH + vr) * DH + c0;
+        float s[4];
+        if (p.state_dtype == KDA_DTYPE_FP32) {
+            const float4 w = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.state) + so);
+            s[0] = w.x; s[1] = w.y; s[2] = w.z; s[3] = w.w;
+        } else {
+            const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.state) + so);
+            s[0] = __uint_as_float(w.x << 16); s[1] = __uint_as_float(w.x & 0xffff0000u);
+            s[2] = __uint_as_float(w.y << 16); s[3] = __uint_as_float(w.y & 0xffff0000u);
+        }
+        float pk = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            s[j] *= alpha[j];
+            pk = fmaf(s[j], kk[j], pk);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) pk += __shfl_xor_sync(0xffffffffu, pk, m);
+        const float w = beta * (bf16_to_f(p.v[tok + vr]) - pk);
+        float o = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            s[j] = fmaf(w, kk[j], s[j]);
+            o = fmaf(s[j], qq[j], o);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) o += __shfl_xor_sync(0xffffffffu, o, m);
+        if (p.state_dtype == KDA_DTYPE_FP32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.state) + so) = make_float4(s[0], s[1], s[2], s[3]);
+        } else {
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.state) + so) =
+                make_uint2(pack_bf16(s[0], s[1]), pack_bf16(s[2], s[3]));
+        }
+        if (lane == 0) p.out[tok + vr] = f2bf_bits(p.scale * o);
+    }
+}
+
+}  // namespace dec
+}  // namespace kda

@@ -58,6 +58,7 @@
 #include "kda_fwd_mma.cuh"
 #include "kda_fwd_tc.cuh"
 #include "kda_probe.cuh"
+#include "kda_decode.cuh"
 
 namespace kda {
 
@@ -292,6 +293,45 @@ KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream)
     return kda_fwd(a->q, a->k, a->v, a->g, a->beta, a->scale, a->out, a->A_log, a->dt_bias, a->lower_bound,
                    a->initial_state, a->initial_dtype, a->final_state, a->final_dtype, a->cu_seqlens, a->N, a->B,
                    a->T, a->H, a->K, a->V, stream);
+}
+
+KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                              void *out, const float *A_log, const float *dt_bias, float lower_bound, void *state,
+                              kda_dtype state_dtype, int64_t S, int64_t H, int64_t K, int64_t V, void *stream)
+{
+    t_last_error.clear();
+    if (K != DH || V != DH) return fail(KDA_ERR_SHAPE, "K and V must be 128 (got K=%lld V=%lld)", (long long)K, (long long)V);
+    if (S < 1 || H < 1 || S * H > (int64_t(1) << 28))
+        return fail(KDA_ERR_SHAPE, "bad sizes S=%lld H=%lld", (long long)S, (long long)H);
+    if (!q || !k || !v || !g || !beta || !out || !state)
+        return fail(KDA_ERR_NULL, "q, k, v, g, beta, out and state are required");
+    if (state_dtype != KDA_DTYPE_BF16 && state_dtype != KDA_DTYPE_FP32)
+        return fail(KDA_ERR_DTYPE, "state dtype must be BF16 or FP32");
+    if (!std::isfinite(lower_bound) || lower_bound < -5.f || lower_bound > 0.f)
+        return fail(KDA_ERR_RANGE, "lower_bound must lie in [-5, 0] (got %g)", (double)lower_bound);
+    if (!std::isfinite(scale)) return fail(KDA_ERR_RANGE, "scale must be finite");
+    if (!aligned(q, 8) || !aligned(k, 8) || !aligned(g, 8) || !aligned(v, 2) || !aligned(beta, 2) || !aligned(out, 2) ||
+        !aligned(state, 16) || (A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+        return fail(KDA_ERR_ALIGN, "q, k, g need 8-byte, state 16-byte and the others natural alignment");
+    dec::DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(v);
+    p.g = static_cast<const uint16_t *>(g);
+    p.beta = static_cast<const uint16_t *>(beta);
+    p.out = static_cast<uint16_t *>(out);
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.state = state;
+    p.state_dtype = state_dtype;
+    p.H = static_cast<int>(H);
+    p.scale = scale;
+    p.lower_bound = lower_bound;
+    const int64_t grid = S * H * (DH / dec::ROWS_PER_CTA);
+    dec::kda_decode_kernel<<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString(e));
+    return KDA_OK;
 }
 
 KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, const void *beta, const float *A_log,

@@ -175,6 +175,30 @@ KDA_API kda_status kda_fwd_host(const void *q, const void *k, const void *v, con
                                 void *stream);
 
 /*
+ * kda_decode -- one token per (sequence, head) against a state updated in
+ * place: the recurrent step that continues a chunked forward pass (its state
+ * is kda_fwd's final_state) ["FlashKDA Input Tensor Shapes and DTypes ..." --
+ * "Initial and Final States": the state carried between calls]. For each of
+ * the S sequences and H heads, with the same gate, beta and scale as kda_fwd:
+ *   S <- S Diag(exp(a)) (I - beta k k^T) + beta v k^T,   out = scale S q.
+ *   q, k, v, g   bf16 [S, H, 128] (DEVICE; kda_fwd's [B, T, H, 128] with T = 1).
+ *   beta         bf16 [S, H] logits.  out  bf16 [S, H, 128], written.
+ *   A_log        fp32 [H] or NULL;    dt_bias  fp32 [H, 128] or NULL.
+ *   state        [S, H, 128 (v), 128 (k)] in state_dtype (BF16 or FP32), read
+ *                and written in place (the caller owns it).
+ * All arithmetic is fp32 (exact sigmoid and exponential); a bf16 state is
+ * rounded to nearest even when stored. Allocates nothing; asynchronous on
+ * `stream`. Errors as kda_fwd: KDA_ERR_SHAPE (K or V != 128, S or H < 1),
+ * KDA_ERR_NULL, KDA_ERR_DTYPE, KDA_ERR_RANGE, KDA_ERR_ALIGN (q, k, g 8-byte,
+ * state 16-byte), KDA_ERR_LAUNCH.
+ */
+KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, float scale, void *out,
+                              const float *A_log, const float *dt_bias, float lower_bound,
+                              void *state, kda_dtype state_dtype,
+                              int64_t S, int64_t H, int64_t K, int64_t V, void *stream);
+
+/*
  * kda_probe_chunk -- test hook: one 16-token chunk of one head through the
  * forward pass's per-chunk steps, built from the same device code as the
  * kernels, so that each step can be checked on its own.

@@ -113,6 +113,28 @@ def test_v_split_override_rejects_bad_values(kda, monkeypatch, value):
     assert _call(kda) == 4  # KDA_ERR_RANGE, before anything touches a GPU
     assert b"KDA_V_SPLIT" in kda.library().kda_last_error()
 
+
+def _decode_call(kda, **over):
+    """Direct kda_decode call with dummy (never dereferenced) aligned pointers."""
+    args = dict(q=0x1000, k=0x2000, v=0x3000, g=0x4000, beta=0x5000, scale=1.0, out=0x6000, A_log=None,
+                dt_bias=None, lb=-5.0, state=0x10000, st_dt=2, S=2, H=3, K=128, V=128, stream=None)
+    args.update(over)
+    return kda.library().kda_decode(*[args[x] for x in ("q", "k", "v", "g", "beta", "scale", "out", "A_log",
+                                                        "dt_bias", "lb", "state", "st_dt", "S", "H", "K", "V",
+                                                        "stream")])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), 2), (dict(V=96), 2), (dict(S=0), 2), (dict(H=0), 2),
+    (dict(q=None), 1), (dict(state=None), 1), (dict(out=None), 1),
+    (dict(st_dt=0), 3), (dict(st_dt=5), 3),
+    (dict(lb=-6.0), 4), (dict(lb=1e-3), 4), (dict(scale=float("nan")), 4),
+    (dict(q=0x1004), 6), (dict(state=0x10008), 6), (dict(out=0x6001), 6),
+])
+def test_decode_host_validation_rejects(kda, over, code):
+    assert _decode_call(kda, **over) == code
+    assert kda.library().kda_last_error()
+
 def test_python_wrapper_rejects_bad_tensors(kda):
     import torch
     q = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16)

@@ -271,3 +271,53 @@ def test_chunk_steps_match_the_fp64_chunk_terms(name, b, h, chunk, rows):
     assert np.all(got["beta"][L:] == 0.0)
     for n, ref in (("A", A), ("P", P), ("T", T)):
         assert_close(n, got[n][:L, :L], ref)
+
+
+
+# ------------------------------------------------------------ single-token steps (decode)
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gate_params", [True, False])
+def test_decode_step_matches_oracle(state_dtype, gate_params):
+    """One token per (sequence, head) with the state updated in place, against the oracle's
+    one-token call from the same initial state."""
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", B=3, T=1, H=5)
+    d["initial_state"] = d["initial_state"].to(state_dtype)
+    if not gate_params:
+        d["A_log"], d["dt_bias"] = None, None
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.full_like(c["v"], float("nan"))
+    state = c["initial_state"].clone()
+    kda.decode(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, state, c["A_log"], c["dt_bias"],
+               d["lower_bound"])
+    kda.check_device_status()
+    o_ref, s_ref = run_oracle(d)
+    assert_close("out", out.float().cpu().double().numpy(), o_ref)
+    assert_close("state", state.float().cpu().double().numpy(), s_ref)
+
+
+def test_decode_steps_continue_the_chunked_pass():
+    """kda_fwd over the first 37 tokens, then ten single-token steps on its final state: the
+    step outputs and the final state match the oracle over all 47 tokens."""
+    import gated_linear_attention_kda_gb300 as kda
+    T0, n = 37, 10
+    d = W.make("b2_t128_h8", T=T0 + n)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    state = torch.empty_like(c["initial_state"])
+    head = {x: c[x][:, :T0].contiguous() for x in ("q", "k", "v", "g", "beta")}
+    out0 = torch.empty_like(head["v"])
+    kda.fwd(head["q"], head["k"], head["v"], head["g"], head["beta"], d["scale"], out0,
+            c["A_log"], c["dt_bias"], d["lower_bound"], c["initial_state"], state)
+    out[:, :T0] = out0
+    for t in range(T0, T0 + n):
+        o_t = torch.empty_like(c["v"][:, t].contiguous())
+        kda.decode(c["q"][:, t].contiguous(), c["k"][:, t].contiguous(), c["v"][:, t].contiguous(),
+                   c["g"][:, t].contiguous(), c["beta"][:, t].contiguous(), d["scale"], o_t, state,
+                   c["A_log"], c["dt_bias"], d["lower_bound"])
+        out[:, t] = o_t
+    kda.check_device_status()
+    o_ref, s_ref = run_oracle(d)
+    assert_close("out", out.float().cpu().double().numpy(), o_ref)
+    assert_close("state", state.cpu().double().numpy(), s_ref)
