@@ -93,6 +93,29 @@ __device__ __forceinline__ Span seq_span(const Params &p, int seq)
     return {seq * p.T, p.T, true};
 }
 
+// Varlen order, longest sequences first: CTA group `rank` (one group per sequence) takes the
+// sequence of that rank in decreasing length, ties by index, so the long sequential chains start
+// in the first wave. Every warp computes it alone (one pass over cu_seqlens per 32 sequences);
+// used for up to 64 sequences, identity beyond. A permutation for any cu_seqlens contents.
+constexpr int LPT_MAX_SEQS = 64;
+__device__ __forceinline__ int lpt_sequence(const Params &p, int rank)
+{
+    const int lane = threadIdx.x & 31;
+    int found = rank;
+    for (int base = 0; base < p.nseq; base += 32) {
+        const int i = base + lane;
+        const long long li = i < p.nseq ? p.cu[i + 1] - p.cu[i] : -1;
+        int r = 0;
+        for (int j = 0; j < p.nseq; ++j) {
+            const long long lj = p.cu[j + 1] - p.cu[j];
+            r += (lj > li) || (lj == li && j < i);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, i < p.nseq && r == rank);
+        if (m) found = base + __ffs(m) - 1;
+    }
+    return found;
+}
+
 // Byte offset of element (row r, channel c) inside a 16x128 bf16 tile loaded
 // as two 64-column boxes with the 128-byte swizzle (16-byte chunk index XOR
 // row mod 8).

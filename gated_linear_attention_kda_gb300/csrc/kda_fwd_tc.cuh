@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // plain C++ shared-memory access at a 32-bit shared address (lets the compiler schedule it)
 #define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int seq = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int h = blockIdx.x % p.H;
+    const int seq = (p.cu && p.nseq <= LPT_MAX_SEQS) ? lpt_sequence(p, blockIdx.x / p.H) : blockIdx.x / p.H;
     const Span sp = seq_span(p, seq);
     if (threadIdx.x == 0) {
         if (p.cu && blockIdx.x == 0 && (p.cu[0] != 0 || p.cu[p.nseq] != p.total)) atomicOr(&g_dev_error, DEVERR_SEQLENS);
