@@ -385,6 +385,55 @@ def run_decode(args):
         "gpu_launches": args.steps}), flush=True)
 
 
+def run_variant(args):
+    """Kernel-only timing of one workload (``--workload``), optionally with raw q/k normalised in
+    the kernel (``--qk-norm``): its own JSON line, tokens/s and the HBM fraction of the
+    algorithmic bytes. Not the benchmark line."""
+    import torch
+
+    import gated_linear_attention_kda_gb300 as kda
+    import workloads as W
+    torch.cuda.set_device(0)
+    name = args.workload or WORKLOAD
+    d = W.make(name, raw_qk=args.qk_norm)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    B, T, H = d["q"].shape[0], d["q"].shape[1], d["q"].shape[2]
+    nseq = B if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    sdt = torch.float32 if d["initial_state"] is None else d["initial_state"].dtype
+    out = torch.empty_like(c["v"])
+    fin = torch.empty(nseq, H, 128, 128, dtype=sdt, device="cuda")
+
+    def step():
+        kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], qk_l2norm=args.qk_norm)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    kda.check_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    st = nseq * H * 128 * 128
+    nbytes = BYTES_PER_TOKEN_HEAD * B * T * H + st * fin.element_size() + (
+        st * d["initial_state"].element_size() if d["initial_state"] is not None else 0)
+    hbm, _, src = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "KDA fwd tokens/s" + (" with q/k L2-normalised in the kernel" if args.qk_norm else ""),
+        "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": name, "B": B, "T": T, "H": H, "sequences": nseq,
+                                        "qk_l2norm": bool(args.qk_norm)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_source": src, "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,12 +444,19 @@ def main():
                     help="profiling mode: run this many forward passes of the workload and exit (no timing)")
     ap.add_argument("--decode", action="store_true",
                     help="time single-token steps (kda_decode) instead and print their own JSON line")
+    ap.add_argument("--workload", default=None,
+                    help="kernel-only timing of another workload (workloads.ORDER) on its own JSON line")
+    ap.add_argument("--qk-norm", action="store_true",
+                    help="kernel-only timing with raw q/k normalised in the kernel (KDA_FLAG_QK_L2NORM)")
     args = ap.parse_args()
     if args.launches:
         run_launches(args.launches)
         return
     if args.decode:
         run_decode(args)
+        return
+    if args.workload or args.qk_norm:
+        run_variant(args)
         return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

@@ -33,6 +33,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE", 4: "KDA_ERR_RANGE",
           5: "KDA_ERR_STATE_MISMATCH", 6: "KDA_ERR_ALIGN", 7: "KDA_ERR_LAUNCH", 8: "KDA_ERR_DEVICE"}
 DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
+FLAG_QK_L2NORM = 1  # KDA_FLAG_QK_L2NORM: q and k L2-normalised per (token, head) inside the kernel
 _P, _F, _I64, _I = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int
 FWD_ARGTYPES = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]
 _lib.kda_fwd.argtypes = FWD_ARGTYPES
@@ -41,6 +42,9 @@ _lib.kda_fwd_host.argtypes = FWD_ARGTYPES
 _lib.kda_fwd_host.restype = _I
 _lib.kda_fwd_flat.argtypes = FWD_ARGTYPES
 _lib.kda_fwd_flat.restype = _I
+FWD_EX_ARGTYPES = FWD_ARGTYPES[:-1] + [ctypes.c_uint32, _P]
+_lib.kda_fwd_ex.argtypes = FWD_EX_ARGTYPES
+_lib.kda_fwd_ex.restype = _I
 
 
 class FwdArgs(ctypes.Structure):
@@ -49,13 +53,16 @@ class FwdArgs(ctypes.Structure):
                 ("A_log", _P), ("dt_bias", _P), ("initial_state", _P), ("final_state", _P),
                 ("cu_seqlens", _P), ("initial_dtype", _I), ("final_dtype", _I),
                 ("scale", _F), ("lower_bound", _F),
-                ("N", _I64), ("B", _I64), ("T", _I64), ("H", _I64), ("K", _I64), ("V", _I64)]
+                ("N", _I64), ("B", _I64), ("T", _I64), ("H", _I64), ("K", _I64), ("V", _I64),
+                ("flags", ctypes.c_uint32)]
 
 
 _lib.kda_fwd_packed.argtypes = [ctypes.POINTER(FwdArgs), _P]
 _lib.kda_fwd_packed.restype = _I
 _lib.kda_decode.argtypes = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _I64, _I64, _I64, _I64, _P]
 _lib.kda_decode.restype = _I
+_lib.kda_decode_ex.argtypes = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _I64, _I64, _I64, _I64, ctypes.c_uint32, _P]
+_lib.kda_decode_ex.restype = _I
 _lib.kda_probe_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P]
 _lib.kda_probe_chunk.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
@@ -139,18 +146,24 @@ def _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
-        initial_state=None, final_state=None, cu_seqlens=None):
+        initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False):
     """Chunked KDA forward on the current CUDA stream. Writes ``out`` (and
-    ``final_state`` if given) in place and returns ``(out, final_state)``."""
+    ``final_state`` if given) in place and returns ``(out, final_state)``.
+    ``qk_l2norm=True`` L2-normalises q and k per (token, head) inside the
+    kernel (``kda_fwd_ex`` with ``KDA_FLAG_QK_L2NORM``); otherwise ``kda_fwd``."""
     B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
                                  cu_seqlens, cuda=True)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+            _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+            _ptr(initial_state), _state_code(initial_state),
+            _ptr(final_state), _state_code(final_state),
+            _ptr(cu_seqlens), N, B, T, H, K, V)
     with torch.cuda.device(q.device):
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-        st = _lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
-                          _ptr(A_log), _ptr(dt_bias), float(lower_bound),
-                          _ptr(initial_state), _state_code(initial_state),
-                          _ptr(final_state), _state_code(final_state),
-                          _ptr(cu_seqlens), N, B, T, H, K, V, ctypes.c_void_p(stream))
+        stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
+        if qk_l2norm:
+            st = _lib.kda_fwd_ex(*args, FLAG_QK_L2NORM, stream)
+        else:
+            st = _lib.kda_fwd(*args, stream)
     _raise(st)
     return out, final_state
 
@@ -172,7 +185,7 @@ def fwd_flat(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound
 
 
 def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
-               initial_state=None, final_state=None, cu_seqlens=None):
+               initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False):
     """``fwd`` through the argument-struct entry point ``kda_fwd_packed``."""
     B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
                                  cu_seqlens, cuda=True)
@@ -184,6 +197,7 @@ def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bou
     a.initial_dtype, a.final_dtype = _state_code(initial_state), _state_code(final_state)
     a.scale, a.lower_bound = float(scale), float(lower_bound)
     a.N, a.B, a.T, a.H, a.K, a.V = N, B, T, H, K, V
+    a.flags = FLAG_QK_L2NORM if qk_l2norm else 0
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = _lib.kda_fwd_packed(ctypes.byref(a), ctypes.c_void_p(stream))
@@ -193,10 +207,11 @@ def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bou
 
 
 
-def decode(q, k, v, g, beta, scale, out, state, A_log=None, dt_bias=None, lower_bound=-5.0):
+def decode(q, k, v, g, beta, scale, out, state, A_log=None, dt_bias=None, lower_bound=-5.0, qk_l2norm=False):
     """One token per (sequence, head) on the current CUDA stream, ``state`` updated in place:
     ``q, k, v, g, out`` bf16 ``[S, H, 128]`` (or ``[S, 1, H, 128]``), ``beta`` bf16 ``[S, H]``
     (or ``[S, 1, H]``), ``state`` bf16/fp32 ``[S, H, 128, 128]`` (kda_fwd's final_state).
+    ``qk_l2norm=True`` L2-normalises q and k inside the kernel (``kda_decode_ex``).
     Returns ``(out, state)``."""
     if not isinstance(q, torch.Tensor) or q.dim() not in (3, 4):
         raise ValueError("q must be [S, H, 128] or [S, 1, H, 128]")
@@ -212,9 +227,9 @@ def decode(q, k, v, g, beta, scale, out, state, A_log=None, dt_bias=None, lower_
     _check("state", state, None, (S, H, V, K), True)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
-        st = _lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
-                             _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(state), _state_code(state),
-                             S, H, K, V, ctypes.c_void_p(stream))
+        st = _lib.kda_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                                _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(state), _state_code(state),
+                                S, H, K, V, FLAG_QK_L2NORM if qk_l2norm else 0, ctypes.c_void_p(stream))
     _raise(st)
     return out, state
 

@@ -25,6 +25,7 @@ struct DecodeParams {
     void *state;                            // [S, H, 128 (V), 128 (K)], fp32 or bf16, in place
     int state_dtype;
     int H;
+    int qk_norm;  // KDA_FLAG_QK_L2NORM: L2-normalise q and k before use
     float scale, lower_bound;
 };
 
@@ -58,6 +59,25 @@ __global__ void __launch_bounds__(THREADS) kda_decode_kernel(const DecodeParams 
             alpha[j] = expf(p.lower_bound * sigmoid_f(ea * (bf16_to_f(gs[j]) + b)));
             kk[j] = bf16_to_f(ks[j]);
             qq[j] = bf16_to_f(qs[j]);
+        }
+    }
+    if (p.qk_norm) {  // x / sqrt(sum x^2 + 1e-6): the warp holds all 128 channels
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            sk = fmaf(kk[j], kk[j], sk);
+            sq = fmaf(qq[j], qq[j], sq);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, m);
+            sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        }
+        const float fk = rsqrtf(sk + 1e-6f), fq = rsqrtf(sq + 1e-6f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kk[j] *= fk;
+            qq[j] *= fq;
         }
     }
     const float beta = sigmoid_f(bf16_to_f(p.beta[unit]));

@@ -119,7 +119,7 @@ static void plan(int64_t units, int num_sms, int *vsplit, int64_t *grid)
     *grid = units * vs;
 }
 
-template <int NS>
+template <int NS, bool QKN>
 static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
                           const CUtensorMap &v, const CUtensorMap &g, const Params &p)
 {
@@ -127,14 +127,16 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(v1::kda_fwd_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, v1::SMEM_ALLOC);
+        cudaError_t e =
+            cudaFuncSetAttribute(v1::kda_fwd_kernel<NS, QKN>, cudaFuncAttributeMaxDynamicSharedMemorySize, v1::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    v1::kda_fwd_kernel<NS><<<static_cast<unsigned>(grid), 32 * (5 + NS), v1::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    v1::kda_fwd_kernel<NS, QKN><<<static_cast<unsigned>(grid), 32 * (5 + NS), v1::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
 }
 
+template <bool QKN>
 static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
                              const CUtensorMap &v, const CUtensorMap &g, const CUtensorMap &o, const Params &p)
 {
@@ -142,13 +144,25 @@ static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q,
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(tcs::kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcs::SMEM_ALLOC);
+        cudaError_t e = cudaFuncSetAttribute(tcs::kda_fwd_tc_kernel<QKN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             tcs::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    tcs::kda_fwd_tc_kernel<<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, o, p);
+    tcs::kda_fwd_tc_kernel<QKN><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, o, p);
     return cudaGetLastError();
+}
+
+template <bool QKN>
+static cudaError_t launch_split(int vs, int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
+                                const CUtensorMap &v, const CUtensorMap &g, const CUtensorMap &o, const Params &p)
+{
+    switch (vs) {
+        case 1: return launch_tc<QKN>(grid, s, q, k, v, g, o, p);
+        case 2: return launch<4, QKN>(grid, s, q, k, v, g, p);
+        case 4: return launch<2, QKN>(grid, s, q, k, v, g, p);
+        default: return launch<1, QKN>(grid, s, q, k, v, g, p);
+    }
 }
 
 static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -176,13 +190,14 @@ KDA_API kda_status kda_plan(int64_t units, int num_sms, int *v_split, int64_t *g
     return KDA_OK;
 }
 
-KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
-                           void *out, const float *A_log, const float *dt_bias, float lower_bound,
-                           const void *initial_state, kda_dtype initial_dtype, void *final_state,
-                           kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
-                           int64_t H, int64_t K, int64_t V, void *stream)
+KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                              const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                              kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                              int64_t H, int64_t K, int64_t V, uint32_t flags, void *stream)
 {
     t_last_error.clear();
+    if (flags & ~KDA_FLAG_QK_L2NORM) return fail(KDA_ERR_RANGE, "unknown option bits 0x%x", flags & ~KDA_FLAG_QK_L2NORM);
     if (K != DH || V != DH) return fail(KDA_ERR_SHAPE, "K and V must be 128 (got K=%lld V=%lld)", (long long)K, (long long)V);
     if (B < 1 || T < 0 || H < 1) return fail(KDA_ERR_SHAPE, "bad sizes B=%lld T=%lld H=%lld", (long long)B, (long long)T, (long long)H);
     if (cu_seqlens && (B != 1 || N < 1))
@@ -267,14 +282,20 @@ KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const vo
     }
     p.vsplit = vs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (vs) {
-        case 1: ce = launch_tc(grid, s, mq, mk, mv, mg, mo, p); break;
-        case 2: ce = launch<4>(grid, s, mq, mk, mv, mg, p); break;
-        case 4: ce = launch<2>(grid, s, mq, mk, mv, mg, p); break;
-        default: ce = launch<1>(grid, s, mq, mk, mv, mg, p); break;
-    }
+    ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, mo, p)
+                                      : launch_split<false>(vs, grid, s, mq, mk, mv, mg, mo, p);
     if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(ce));
     return KDA_OK;
+}
+
+KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                           void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                           const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                           kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                           int64_t H, int64_t K, int64_t V, void *stream)
+{
+    return kda_fwd_ex(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype,
+                      final_state, final_dtype, cu_seqlens, N, B, T, H, K, V, 0u, stream);
 }
 
 KDA_API kda_status kda_fwd_flat(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -290,16 +311,18 @@ KDA_API kda_status kda_fwd_flat(const void *q, const void *k, const void *v, con
 KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream)
 {
     if (!a) return fail(KDA_ERR_NULL, "kda_fwd_packed: NULL argument struct");
-    return kda_fwd(a->q, a->k, a->v, a->g, a->beta, a->scale, a->out, a->A_log, a->dt_bias, a->lower_bound,
-                   a->initial_state, a->initial_dtype, a->final_state, a->final_dtype, a->cu_seqlens, a->N, a->B,
-                   a->T, a->H, a->K, a->V, stream);
+    return kda_fwd_ex(a->q, a->k, a->v, a->g, a->beta, a->scale, a->out, a->A_log, a->dt_bias, a->lower_bound,
+                      a->initial_state, a->initial_dtype, a->final_state, a->final_dtype, a->cu_seqlens, a->N, a->B,
+                      a->T, a->H, a->K, a->V, a->flags, stream);
 }
 
-KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
-                              void *out, const float *A_log, const float *dt_bias, float lower_bound, void *state,
-                              kda_dtype state_dtype, int64_t S, int64_t H, int64_t K, int64_t V, void *stream)
+KDA_API kda_status kda_decode_ex(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                 float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                                 void *state, kda_dtype state_dtype, int64_t S, int64_t H, int64_t K, int64_t V,
+                                 uint32_t flags, void *stream)
 {
     t_last_error.clear();
+    if (flags & ~KDA_FLAG_QK_L2NORM) return fail(KDA_ERR_RANGE, "unknown option bits 0x%x", flags & ~KDA_FLAG_QK_L2NORM);
     if (K != DH || V != DH) return fail(KDA_ERR_SHAPE, "K and V must be 128 (got K=%lld V=%lld)", (long long)K, (long long)V);
     if (S < 1 || H < 1 || S * H > (int64_t(1) << 28))
         return fail(KDA_ERR_SHAPE, "bad sizes S=%lld H=%lld", (long long)S, (long long)H);
@@ -327,11 +350,20 @@ KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const
     p.H = static_cast<int>(H);
     p.scale = scale;
     p.lower_bound = lower_bound;
+    p.qk_norm = (flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     const int64_t grid = S * H * (DH / dec::ROWS_PER_CTA);
     dec::kda_decode_kernel<<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString(e));
     return KDA_OK;
+}
+
+KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                              void *out, const float *A_log, const float *dt_bias, float lower_bound, void *state,
+                              kda_dtype state_dtype, int64_t S, int64_t H, int64_t K, int64_t V, void *stream)
+{
+    return kda_decode_ex(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, state, state_dtype, S, H, K, V, 0u,
+                         stream);
 }
 
 KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, const void *beta, const float *A_log,

@@ -29,7 +29,8 @@ constexpr int S_QLL = S_QLH + 16 * H_LD;
 constexpr int S_KRH = S_QLL + 16 * H_LD;
 constexpr int S_KRL = S_KRH + 16 * H_LD;
 constexpr int S_BETA = S_KRL + 16 * H_LD;
-constexpr int SCR = S_BETA + 64;
+constexpr int S_NRM = S_BETA + 64;    // f32 [2 warps][32]: row sums of squares of k (rows 0-15) and q (16-31)
+constexpr int SCR = S_NRM + 256;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_PREP = OFF_RAW + NR * RAW_STAGE;
@@ -44,7 +45,37 @@ static_assert(PREP_SLOT % 16 == 0 && SCR % 16 == 0 && OFF_PREP % 1024 == 0, "ali
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-template <int NS>
+// L2 scale factor 1 / sqrt(sum x^2 + 1e-6) of k row `lane` (lanes 0-15) or q row `lane - 16`
+// (lanes 16-31) of a prep lane's chunk: each thread holds two channels of every row, a warp 64
+// channels. The 32 per-thread sums of squares go through a reduce-scatter butterfly (lane l
+// ends with its warp's sum of value l), the two warps' halves meet in shared memory.
+__device__ __forceinline__ float qk_row_scale64(const uint32_t (&kw)[CHUNK], const uint32_t (&qw)[CHUNK], int lane,
+                                                int lw, uint8_t *nrm, uint32_t bar_id)
+{
+    float v[32];
+#pragma unroll
+    for (int r = 0; r < CHUNK; ++r) {
+        const float k0 = bf16_lo(kw[r]), k1 = bf16_hi(kw[r]), q0 = bf16_lo(qw[r]), q1 = bf16_hi(qw[r]);
+        v[r] = fmaf(k0, k0, k1 * k1);
+        v[CHUNK + r] = fmaf(q0, q0, q1 * q1);
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = lane & w;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float keep = up ? v[i + w] : v[i], send = up ? v[i] : v[i + w];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    reinterpret_cast<float *>(nrm)[32 * lw + lane] = v[0];
+    named_bar_sync(bar_id, 64);
+    const float tot = reinterpret_cast<const float *>(nrm)[lane] + reinterpret_cast<const float *>(nrm)[32 + lane];
+    return rsqrtf(tot + 1e-6f);
+}
+
+// QKN: L2-normalise the q and k rows in the element-wise pass (KDA_FLAG_QK_L2NORM).
+template <int NS, bool QKN>
 __global__ void __launch_bounds__(32 * (5 + NS), 1)
     kda_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
@@ -173,12 +204,21 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
                 kwv[r] = SM_AT(const uint32_t, raw + OFF_K + raw_off(r, c0));
                 qwv[r] = SM_AT(const uint32_t, raw + OFF_Q + raw_off(r, c0));
             }
+            float fqk = 1.f;
+            if constexpr (QKN) fqk = qk_row_scale64(kwv, qwv, lane, lw, smem + (scr + S_NRM - sb), bar_id);
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
                 const uint32_t kw = kwv[r], qw = qwv[r];
                 const bool live = r < Lv;
-                const float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
-                const float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
+                float k0 = live ? bf16_lo(kw) : 0.f, k1 = live ? bf16_hi(kw) : 0.f;
+                float q0 = live ? bf16_lo(qw) : 0.f, q1 = live ? bf16_hi(qw) : 0.f;
+                if constexpr (QKN) {
+                    const float fk = __shfl_sync(0xffffffffu, fqk, r), fq = __shfl_sync(0xffffffffu, fqk, CHUNK + r);
+                    k0 *= fk;
+                    k1 *= fk;
+                    q0 *= fq;
+                    q1 *= fq;
+                }
                 const float gm0 = ex2_approx(G0[r]), gm1 = ex2_approx(G1[r]);            // Gamma_r
                 const float f0 = ex2_approx(Gm0 - G0[r]), f1 = ex2_approx(Gm1 - G1[r]);  // 2^(G_mid - G_r)
                 SM_AT(uint32_t, pslot + P_BZ + r * BZ_LD + c0 * 2) = pack_bf16(k0 * gm0, k1 * gm1);

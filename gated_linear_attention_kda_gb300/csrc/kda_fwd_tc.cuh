@@ -155,6 +155,42 @@ __device__ __noinline__ void issue_d(uint32_t tmem, uint32_t sl, int dbuf, int b
     for (int i = 0; i < 4; ++i) tc::mma_ts_tf32(dn, x + 8 * i, dp + ((256 * i) >> 4), id_p, 1);
 }
 
+// L2 scale factors 1 / sqrt(sum x^2 + 1e-6) of the four k rows and four q rows held by this
+// warp (a thread holds 4 channels of each row, the warp all 128). The eight sums of squares
+// are reduced in a reduce-scatter butterfly (each exchange halves the values a lane keeps),
+// so lane l ends with the full sum of value (l >> 2): k rows 0..3, then q rows 0..3.
+__device__ __forceinline__ void qk_row_scales(const uint2 (&kw)[4], const uint2 (&qw)[4], int lane, float (&sk)[4],
+                                              float (&sq)[4])
+{
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float k0 = bf16_lo(kw[i].x), k1 = bf16_hi(kw[i].x), k2 = bf16_lo(kw[i].y), k3 = bf16_hi(kw[i].y);
+        const float q0 = bf16_lo(qw[i].x), q1 = bf16_hi(qw[i].x), q2 = bf16_lo(qw[i].y), q3 = bf16_hi(qw[i].y);
+        v[i] = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, k3 * k3)));
+        v[4 + i] = fmaf(q0, q0, fmaf(q1, q1, fmaf(q2, q2, q3 * q3)));
+    }
+#pragma unroll
+    for (int w = 16, n = 4; w >= 4; w >>= 1, n >>= 1) {
+        const bool up = lane & w;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float keep = up ? v[i + n] : v[i], send = up ? v[i] : v[i + n];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    const float f = rsqrtf(v[0] + 1e-6f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        sk[i] = __shfl_sync(0xffffffffu, f, 4 * i);
+        sq[i] = __shfl_sync(0xffffffffu, f, 16 + 4 * i);
+    }
+}
+
+// QKN: L2-normalise the q and k rows in the element-wise pass (KDA_FLAG_QK_L2NORM).
+template <bool QKN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -575,11 +611,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qwv[i] = SM_AT(const uint2, raw + OFF_Q + raw_off(r, c0));
                 vwv[i] = SM_AT(const uint2, raw + OFF_V + raw_off(r, c0));
             }
+            float sk[4], sq[4];
+            if constexpr (QKN) qk_row_scales(kwv, qwv, lane, sk, sq);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = r0 + i;
-                const float k[4] = {bf16_lo(kwv[i].x), bf16_hi(kwv[i].x), bf16_lo(kwv[i].y), bf16_hi(kwv[i].y)};
-                const float q[4] = {bf16_lo(qwv[i].x), bf16_hi(qwv[i].x), bf16_lo(qwv[i].y), bf16_hi(qwv[i].y)};
+                float k[4] = {bf16_lo(kwv[i].x), bf16_hi(kwv[i].x), bf16_lo(kwv[i].y), bf16_hi(kwv[i].y)};
+                float q[4] = {bf16_lo(qwv[i].x), bf16_hi(qwv[i].x), bf16_lo(qwv[i].y), bf16_hi(qwv[i].y)};
+                if constexpr (QKN) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        k[j] *= sk[i];
+                        q[j] *= sq[i];
+                    }
+                }
                 float kl[4], ql[4], kr[4], kg[4], qg[4], kb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {

@@ -75,6 +75,19 @@ typedef enum kda_dtype {
 } kda_dtype;
 
 /*
+ * Option bits of kda_fwd_ex, kda_decode_ex and kda_fwd_args.flags (0 selects
+ * the plain behaviour of kda_fwd / kda_decode).
+ *   KDA_FLAG_QK_L2NORM  L2-normalise every (token, head) vector of q and k
+ *                       inside the kernel before it is used:
+ *                         x[c] <- x[c] / sqrt(sum_c' x[c']^2 + 1e-6)
+ *                       in fp32 from the bf16 inputs (the inputs are not
+ *                       modified). The pages do not say whether q and k arrive
+ *                       normalised; without this bit they are used as given.
+ * Any other bit is KDA_ERR_RANGE.
+ */
+#define KDA_FLAG_QK_L2NORM 1u
+
+/*
  * kda_fwd -- the chunked KDA forward pass (CHUNK = 16 [CHUNK]).
  *
  * Tensors (all row-major, contiguous, DEVICE memory):
@@ -135,6 +148,19 @@ KDA_API kda_status kda_fwd_flat(const void *q, const void *k, const void *v, con
                                 void *stream);
 
 /*
+ * kda_fwd_ex -- kda_fwd with option bits (`flags`, see KDA_FLAG_QK_L2NORM);
+ * every other argument, check and error is kda_fwd's. flags == 0 is kda_fwd.
+ */
+KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, float scale, void *out,
+                              const float *A_log, const float *dt_bias, float lower_bound,
+                              const void *initial_state, kda_dtype initial_dtype,
+                              void *final_state, kda_dtype final_dtype,
+                              const int64_t *cu_seqlens, int64_t N,
+                              int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                              uint32_t flags, void *stream);
+
+/*
  * kda_fwd_args / kda_fwd_packed -- the same operation with its arguments in
  * one struct. Every field has the meaning, layout and ownership of the
  * kda_fwd argument of the same name; the struct itself is read during the
@@ -152,6 +178,7 @@ typedef struct kda_fwd_args {
     kda_dtype initial_dtype, final_dtype;
     float scale, lower_bound;
     int64_t N, B, T, H, K, V;
+    uint32_t flags;                    /* KDA_FLAG_* bits, as kda_fwd_ex; 0 for kda_fwd */
 } kda_fwd_args;
 
 KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream);
@@ -197,6 +224,17 @@ KDA_API kda_status kda_decode(const void *q, const void *k, const void *v, const
                               const float *A_log, const float *dt_bias, float lower_bound,
                               void *state, kda_dtype state_dtype,
                               int64_t S, int64_t H, int64_t K, int64_t V, void *stream);
+
+/*
+ * kda_decode_ex -- kda_decode with option bits (`flags`, see
+ * KDA_FLAG_QK_L2NORM); everything else is kda_decode's.
+ */
+KDA_API kda_status kda_decode_ex(const void *q, const void *k, const void *v, const void *g,
+                                 const void *beta, float scale, void *out,
+                                 const float *A_log, const float *dt_bias, float lower_bound,
+                                 void *state, kda_dtype state_dtype,
+                                 int64_t S, int64_t H, int64_t K, int64_t V, uint32_t flags,
+                                 void *stream);
 
 /*
  * kda_probe_chunk -- test hook: one 16-token chunk of one head through the

@@ -40,7 +40,7 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
-        lib.kda_oracle_fwd.argtypes = [P, P, P, P, P, D, P, P, P, D, P, P, P, I, I, I, I, I, I, I]
+        lib.kda_oracle_fwd.argtypes = [P, P, P, P, P, D, P, P, P, D, P, P, P, I, I, I, I, I, I, I, I]
         lib.kda_oracle_fwd.restype = I
         lib.kda_oracle_core.argtypes = [P, P, P, P, P, D, P, P, P, P, I, I, I, I, I, I, I]
         lib.kda_oracle_core.restype = I
@@ -63,12 +63,13 @@ def default_threads() -> int:
 
 
 def fwd(q, k, v, g, beta, scale, A_log=None, dt_bias=None, lower_bound=-5.0,
-        initial_state=None, cu_seqlens=None, nthreads=None):
+        initial_state=None, cu_seqlens=None, nthreads=None, qk_l2norm=False):
     """Per-token fp64 forward.
 
     ``q, k, v, g``: uint16 bf16 bit patterns ``[B, T, H, K|V]``; ``beta``: uint16
     ``[B, T, H]`` logits; ``A_log`` float32 ``[H]``; ``dt_bias`` float32 ``[H, K]``;
     ``initial_state`` float64 ``[B|N, H, V, K]``; ``cu_seqlens`` int64 ``[N+1]``.
+    ``qk_l2norm``: L2-normalise q and k per (token, head), ``x / sqrt(sum x^2 + 1e-6)``.
     Returns ``(out float64 [B,T,H,V], final_state float64 [B|N,H,V,K])``.
     """
     q, k, v, g, beta = (_c(x, np.uint16) for x in (q, k, v, g, beta))
@@ -83,7 +84,7 @@ def fwd(q, k, v, g, beta, scale, A_log=None, dt_bias=None, lower_bound=-5.0,
     rc = _load().kda_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
                                 _ptr(_c(A_log, np.float32)), _ptr(_c(dt_bias, np.float32)),
                                 float(lower_bound), _ptr(init), _ptr(fin), _ptr(cu),
-                                B, T, H, K, V, N, int(nthreads or default_threads()))
+                                B, T, H, K, V, N, int(bool(qk_l2norm)), int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out, fin

@@ -39,6 +39,12 @@
  *    from its own initial state.
  *
  * bf16 inputs arrive as raw 16-bit patterns and are widened exactly.
+ *
+ * Optional (qk_l2norm != 0): every (token, head) vector of q and k is first
+ * L2-normalised, x[c] <- x[c] / sqrt(sum_c' x[c']^2 + 1e-6). The pages do not
+ * say whether q and k arrive normalised (their examples draw them from randn);
+ * this option is the library's KDA_FLAG_QK_L2NORM, with the epsilon placed
+ * inside the square root.
  */
 #include <math.h>
 #include <stdint.h>
@@ -154,6 +160,7 @@ int kda_oracle_gate(const uint16_t *g, const float *A_log, const float *dt_bias,
  *   dt_bias: [H, K] fp32 or NULL;  out: [B, T, H, V] fp64;
  *   initial_state / final_state: [B|N, H, V, K] fp64 or NULL;
  *   cu_seqlens: [N+1] or NULL (then B == 1 and T is the packed length).
+ *   qk_l2norm: nonzero to L2-normalise q and k per (token, head) first.
  * Returns 0, or -1 on bad arguments.
  */
 int kda_oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -161,7 +168,7 @@ int kda_oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                    double *out, const float *A_log, const float *dt_bias,
                    double lower_bound, const double *initial_state,
                    double *final_state, const int64_t *cu_seqlens, int B, int T,
-                   int H, int K, int V, int N, int nthreads)
+                   int H, int K, int V, int N, int qk_l2norm, int nthreads)
 {
     if (!q || !k || !v || !g || !beta || !out)
         return -1;
@@ -200,6 +207,18 @@ int kda_oracle_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 alpha[c] = exp(lower_bound * sigmoid(xg[c]));
                 kk[c] = widen_bf16(k[rk + c]);
                 qq[c] = widen_bf16(q[rk + c]);
+            }
+            if (qk_l2norm) {
+                double sk = 0.0, sq = 0.0;
+                for (int c = 0; c < K; c++) {
+                    sk += kk[c] * kk[c];
+                    sq += qq[c] * qq[c];
+                }
+                double fk = 1.0 / sqrt(sk + 1e-6), fq = 1.0 / sqrt(sq + 1e-6);
+                for (int c = 0; c < K; c++) {
+                    kk[c] *= fk;
+                    qq[c] *= fq;
+                }
             }
             for (int r = 0; r < V; r++)
                 vv[r] = widen_bf16(v[rv + r]);

@@ -16,7 +16,7 @@ def to_dev(d, dev="cuda"):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None):
+def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None, qk_l2norm=False):
     import gated_linear_attention_kda_gb300 as kda
     c = to_dev(d)
     out = torch.full_like(c["v"], float("nan"))
@@ -30,14 +30,14 @@ def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None)
         fin = torch.full((nseq, H, 128, 128), float("nan"), dtype=_DT[final_dtype], device="cuda")
     kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"] if scale is None else scale, out,
             c["A_log"], c["dt_bias"], d["lower_bound"] if lower_bound is None else lower_bound, init, fin,
-            c["cu_seqlens"])
+            c["cu_seqlens"], qk_l2norm=qk_l2norm)
     kda.check_device_status()
     o = out.float().cpu().double().numpy()
     s = None if fin is None else fin.float().cpu().double().numpy()
     return o, s
 
 
-def run_oracle(d, heads=None, lower_bound=None, scale=None):
+def run_oracle(d, heads=None, lower_bound=None, scale=None, qk_l2norm=False):
     """fp64 oracle; ``heads`` restricts the run to those heads (heads are independent)."""
     sel = (lambda x: x) if heads is None else (lambda x: x[:, :, heads])
     bits = {k: W.bf16_bits(sel(d[k]).contiguous()) for k in ("q", "k", "v", "g")}
@@ -50,7 +50,8 @@ def run_oracle(d, heads=None, lower_bound=None, scale=None):
     cu = None if d["cu_seqlens"] is None else d["cu_seqlens"].numpy()
     return oracle.fwd(bits["q"], bits["k"], bits["v"], bits["g"], bb,
                       d["scale"] if scale is None else scale, A, db,
-                      d["lower_bound"] if lower_bound is None else lower_bound, W.state_f64(init), cu)
+                      d["lower_bound"] if lower_bound is None else lower_bound, W.state_f64(init), cu,
+                      qk_l2norm=qk_l2norm)
 
 
 def assert_close(name, got, ref, rel_l2=REL_L2):

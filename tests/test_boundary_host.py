@@ -107,6 +107,25 @@ def test_host_validation_rejects(kda, over, code):
 
 
 
+@pytest.mark.parametrize("flags", [2, 4, 0x80000000, 3])
+def test_unknown_option_bits_are_rejected_on_the_host(kda, flags):
+    lib = kda.library()
+    st = lib.kda_fwd_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0,
+                        None, 0, 1, 16, 1, 128, 128, flags, None)
+    assert st == 4 and b"option bits" in lib.kda_last_error()
+    st = lib.kda_decode_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, 0x10000, 2,
+                           2, 3, 128, 128, flags, None)
+    assert st == 4 and b"option bits" in lib.kda_last_error()
+
+
+def test_option_entry_points_validate_like_the_plain_ones(kda):
+    lib = kda.library()
+    assert lib.kda_fwd_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0,
+                          None, 0, 1, 16, 1, 64, 128, 1, None) == 2  # K != 128 with the flag set
+    assert lib.kda_decode_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 2,
+                             2, 3, 128, 128, 1, None) == 1  # state NULL
+
+
 @pytest.mark.parametrize("value", ["3", "0", "16", "x"])
 def test_v_split_override_rejects_bad_values(kda, monkeypatch, value):
     monkeypatch.setenv("KDA_V_SPLIT", value)

@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 
 def _check(d, final_dtype="fp32", heads=None, **kw):
     o, s = run_gpu(d, final_dtype=final_dtype, **kw)
-    o_ref, s_ref = run_oracle(d, heads=heads, lower_bound=kw.get("lower_bound"), scale=kw.get("scale"))
+    o_ref, s_ref = run_oracle(d, heads=heads, lower_bound=kw.get("lower_bound"), scale=kw.get("scale"),
+                              qk_l2norm=kw.get("qk_l2norm", False))
     if heads is not None:
         o, s = o[:, :, heads], (None if s is None else s[:, heads])
     rel = assert_close("out", o, o_ref)
@@ -274,6 +275,51 @@ def test_chunk_steps_match_the_fp64_chunk_terms(name, b, h, chunk, rows):
 
 
 
+# ------------------------------------------------------------ q/k L2 normalisation in the kernel
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+@pytest.mark.parametrize("T", [37, 128])
+def test_qk_l2norm_in_kernel_matches_oracle(T, H):
+    """Raw N(0, 1) q and k (norms near sqrt(128)), normalised inside the kernel
+    (KDA_FLAG_QK_L2NORM), against the oracle with the same normalisation; both kernels."""
+    d = W.make("b2_t128_h8", B=1, T=T, H=H, raw_qk=True)
+    _check(d, heads=None if H < 8 else [0, 41, 79], qk_l2norm=True)
+
+
+@pytest.mark.parametrize("H", KERNEL_HEADS)
+def test_qk_l2norm_varlen_ragged_and_empty(H):
+    d = W.make("varlen_n16_h32", lengths=[0, 19, 64, 1, 33], H=H, raw_qk=True)
+    _check(d, final_dtype="bf16", heads=None if H < 8 else [3, 77], qk_l2norm=True)
+
+
+def test_qk_l2norm_flag_through_struct_entry():
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", B=1, T=45, H=80, raw_qk=True)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    outs = []
+    for fn in (kda.fwd, kda.fwd_packed):
+        out = torch.full_like(c["v"], float("nan"))
+        fin = torch.full_like(c["initial_state"], float("nan"))
+        fn(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+           d["lower_bound"], c["initial_state"], fin, qk_l2norm=True)
+        outs.append((out, fin))
+    kda.check_device_status()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_unknown_option_bits_are_rejected():
+    import ctypes
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b1_t64_h1")
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    st = kda.library().kda_fwd_ex(P(c["q"]), P(c["k"]), P(c["v"]), P(c["g"]), P(c["beta"]), d["scale"], P(out),
+                                  P(c["A_log"]), P(c["dt_bias"]), d["lower_bound"], None, 0, None, 0, None, 0,
+                                  1, 64, 1, 128, 128, 6, None)
+    assert st == 4  # KDA_ERR_RANGE
+
+
 # ------------------------------------------------------------ single-token steps (decode)
 
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
@@ -293,6 +339,20 @@ def test_decode_step_matches_oracle(state_dtype, gate_params):
                d["lower_bound"])
     kda.check_device_status()
     o_ref, s_ref = run_oracle(d)
+    assert_close("out", out.float().cpu().double().numpy(), o_ref)
+    assert_close("state", state.float().cpu().double().numpy(), s_ref)
+
+
+def test_decode_step_qk_l2norm_matches_oracle():
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", B=3, T=1, H=5, raw_qk=True)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.full_like(c["v"], float("nan"))
+    state = c["initial_state"].clone()
+    kda.decode(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, state, c["A_log"], c["dt_bias"],
+               d["lower_bound"], qk_l2norm=True)
+    kda.check_device_status()
+    o_ref, s_ref = run_oracle(d, qk_l2norm=True)
     assert_close("out", out.float().cpu().double().numpy(), o_ref)
     assert_close("state", state.float().cpu().double().numpy(), s_ref)
 

@@ -31,6 +31,9 @@ MUTANTS = {
     "beta_not_activated": ("double bt = sigmoid(widen_bf16(beta[(size_t)t * H + h]));",
                            "double bt = widen_bf16(beta[(size_t)t * H + h]);"),
     "varlen_state_slot": ("*slot = seq;", "*slot = 0;"),
+    "qk_norm_skips_q": ("qq[c] *= fq;", "qq[c] *= 1.0;"),
+    "qk_norm_no_sqrt": ("double fk = 1.0 / sqrt(sk + 1e-6), fq = 1.0 / sqrt(sq + 1e-6);",
+                        "double fk = 1.0 / (sk + 1e-6), fq = 1.0 / (sq + 1e-6);"),
     "gate_entry_A_log": ("double a = A_log ? exp((double)A_log[h]) : 1.0;\n            for (int c",
                          "double a = A_log ? (double)A_log[h] : 1.0;\n            for (int c"),
 }
@@ -47,6 +50,8 @@ PIN_TESTS = [
     pins.test_varlen_equals_separate_calls,
     pins.test_split_call_state_carry,
     pins.test_scale_is_linear_on_output_only,
+    pins.test_qk_l2norm_invariant_to_power_of_two_input_scale,
+    pins.test_qk_l2norm_delta_rule_storage_with_scaled_one_hot_keys,
 ]
 
 

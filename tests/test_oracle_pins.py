@@ -135,6 +135,53 @@ def test_delta_rule_storage_through_full_gate():
     np.testing.assert_allclose(out[0, :, 0], vals, rtol=0, atol=0)
 
 
+# ---------------------------------------------------------------- in-kernel q/k normalisation
+
+def test_qk_l2norm_invariant_to_power_of_two_input_scale():
+    """With q and k L2-normalised first, multiplying every q by 4 and every k by 1/2 (exact in
+    bf16) leaves the forward pass unchanged up to the 1e-6 inside the square root; without the
+    normalisation the same rescaling changes it."""
+    d, bits, A, db, init, cu = _inputs("b2_t128_h8", T=40, H=2, raw_qk=True)
+    q, k = _f64(bits["q"]), _f64(bits["k"])
+    scaled = dict(bits, q=_bits(4.0 * q), k=_bits(0.5 * k))
+    np.testing.assert_array_equal(_f64(scaled["q"]), 4.0 * q)   # the rescaling is exact
+    np.testing.assert_array_equal(_f64(scaled["k"]), 0.5 * k)
+    args = (d["scale"], A, db, d["lower_bound"], init, cu)
+    o1, s1 = oracle.fwd(bits["q"], bits["k"], bits["v"], bits["g"], bits["beta"], *args, qk_l2norm=True)
+    o2, s2 = oracle.fwd(scaled["q"], scaled["k"], bits["v"], bits["g"], bits["beta"], *args, qk_l2norm=True)
+    np.testing.assert_allclose(o2, o1, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(s2, s1, rtol=1e-6, atol=1e-9)
+    o3, _ = oracle.fwd(bits["q"], bits["k"], bits["v"], bits["g"], bits["beta"], *args)
+    o4, _ = oracle.fwd(scaled["q"], scaled["k"], bits["v"], bits["g"], bits["beta"], *args)
+    assert np.abs(o4 - o3).max() > 1e-2
+
+
+def test_qk_l2norm_delta_rule_storage_with_scaled_one_hot_keys():
+    """lower_bound = 0 (no decay), beta = 1, keys c_j e_j on distinct channels: the normalised
+    key is a_j e_j with a_j = c_j / sqrt(c_j^2 + 1e-6), so the delta rule leaves S e_j = a_j v_j,
+    and a later query d_j e_j (with k = 0, which the normalisation keeps at 0) reads
+    scale * a_j * b_j * v_j with b_j = d_j / sqrt(d_j^2 + 1e-6)."""
+    K = V = 128
+    n = 12
+    keys = np.zeros((2 * n, K))
+    qrys = np.zeros((2 * n, K))
+    for j in range(n):
+        keys[j, 5 * j + 1] = (2.0, 8.0, 16.0)[j % 3]
+        qrys[n + j, 5 * j + 1] = (4.0, 0.5, 32.0)[j % 3]
+        qrys[j, 0] = 1.0
+    vals = _f64(_bits(rng.standard_normal((2 * n, V))))
+    g = _bits(rng.standard_normal((1, 2 * n, 1, K)))
+    out, fin = oracle.fwd(_bits(qrys[None, :, None]), _bits(keys[None, :, None]), _bits(vals[None, :, None]), g,
+                          _bits(np.full((1, 2 * n, 1), np.inf)), 0.5, None, None, 0.0, None, None, qk_l2norm=True)
+    c = keys[:n].sum(axis=1)
+    dq = qrys[n:].sum(axis=1)
+    a = c / np.sqrt(c * c + 1e-6)
+    b = dq / np.sqrt(dq * dq + 1e-6)
+    np.testing.assert_allclose(out[0, n:, 0], 0.5 * (a * b)[:, None] * vals[:n], rtol=1e-12, atol=1e-14)
+    unit = (keys[:n] != 0).astype(np.float64)
+    np.testing.assert_allclose(fin[0, 0] @ unit.T, (a[:, None] * vals[:n]).T, rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------- gate
 
 def test_gate_special_points():

@@ -7,7 +7,8 @@ their inputs from here, as identical bytes.
 Recipe (one ``torch.Generator`` on the CPU, seeded per workload; draws in this
 fixed order: [varlen lengths], q, k, v, g, beta, A_log, dt_bias, initial_state):
 
-* q, k ~ N(0, 1) in fp32, L2-normalised per (token, head) vector, then bf16;
+* q, k ~ N(0, 1) in fp32, L2-normalised per (token, head) vector, then bf16
+  (``raw_qk=True`` keeps the raw N(0, 1) draws, for the in-kernel normalisation);
 * v, g, beta logits ~ N(0, 1), then bf16;
 * A_log ~ U(0, ln 16) fp32 ``[H]``; dt_bias ~ N(0, 0.1^2) fp32 ``[H, 128]``;
 * initial_state ~ N(0, 0.02^2) in its stated dtype;
@@ -74,11 +75,12 @@ def varlen_lengths(gen: torch.Generator, n: int, max_len: int):
 
 
 def make(w, seed: Optional[int] = None, T: Optional[int] = None, H: Optional[int] = None,
-         B: Optional[int] = None, lengths=None) -> dict:
+         B: Optional[int] = None, lengths=None, raw_qk: bool = False) -> dict:
     """Build the CPU tensors of a workload (by name or ``Workload``).
 
     ``T``/``H``/``B``/``lengths`` override the shape for reduced parity cases;
-    ``lengths`` (a list) makes a varlen case. Returns a dict with keys ``q k v g
+    ``lengths`` (a list) makes a varlen case; ``raw_qk`` skips the L2 normalisation
+    of q and k (same random draws). Returns a dict with keys ``q k v g
     beta A_log dt_bias initial_state cu_seqlens scale lower_bound final_dtype``.
     """
     if isinstance(w, str):
@@ -98,8 +100,9 @@ def make(w, seed: Optional[int] = None, T: Optional[int] = None, H: Optional[int
     else:
         T = w.T if T is None else T
     D = HEAD_DIM
-    q = _l2n(torch.randn(B, T, H, D, generator=gen)).to(torch.bfloat16)
-    k = _l2n(torch.randn(B, T, H, D, generator=gen)).to(torch.bfloat16)
+    nrm = (lambda x: x) if raw_qk else _l2n
+    q = nrm(torch.randn(B, T, H, D, generator=gen)).to(torch.bfloat16)
+    k = nrm(torch.randn(B, T, H, D, generator=gen)).to(torch.bfloat16)
     v = torch.randn(B, T, H, D, generator=gen).to(torch.bfloat16)
     g = torch.randn(B, T, H, D, generator=gen).to(torch.bfloat16)
     beta = torch.randn(B, T, H, generator=gen).to(torch.bfloat16)
