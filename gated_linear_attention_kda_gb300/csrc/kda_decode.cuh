@@ -25,13 +25,14 @@ struct DecodeParams {
     void *state;                            // [S, H, 128 (V), 128 (K)], fp32 or bf16, in place
     int state_dtype;
     int H;
-    int qk_norm;  // KDA_FLAG_QK_L2NORM: L2-normalise q and k before use
     float scale, lower_bound;
 };
 
 __device__ __forceinline__ float bf16_to_f(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 
+// QKN: L2-normalise q and k before use (KDA_FLAG_QK_L2NORM).
+template <bool QKN>
 __global__ void __launch_bounds__(THREADS) kda_decode_kernel(const DecodeParams p)
 {
     const int unit = blockIdx.x / (DH / ROWS_PER_CTA);  // (sequence, head)
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(THREADS) kda_decode_kernel(const DecodeParams 
             qq[j] = bf16_to_f(qs[j]);
         }
     }
-    if (p.qk_norm) {  // x / sqrt(sum x^2 + 1e-6): the warp holds all 128 channels
+    if constexpr (QKN) {  // x / sqrt(sum x^2 + 1e-6): the warp holds all 128 channels
         float sk = 0.f, sq = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -3,20 +3,23 @@
 //
 // One CTA owns one (sequence, head) state, or a slice of its V rows when there
 // are too few states to fill the machine (the rows of S are independent).
-// Warp roles inside the CTA:
-//   warp 0       TMA producer: streams the 16-token q/k/v/g tiles of each
-//                chunk into a 6-deep shared-memory ring.
-//   warps 1..4   two "prep lanes" of two warps each, working on alternate
-//                chunks: gate activation in base 2, in-chunk cumsum, the
-//                exponent-scaled operand tiles, the 16x16 chunk matrix A and
-//                the intra-chunk score matrix P (tf32 MMA), and the
-//                unit-lower inverse T = (I + A)^-1 by forward substitution.
-//   warps 5..    scan warps, 16 V rows each, holding their rows of the fp32
-//                state S in registers across the whole sequence. Per chunk:
-//                  Z   = S [K*Gamma ; Q*Gamma]^T              (bf16 MMA)
-//                  R   = V^T - Z_k,  E = R (T diag(beta))^T   (fp16 MMA)
-//                  O   = scale (Z_q + E P^T)                  (fp16 MMA)
-//                  S   = S Diag(gamma) + E Kbar               (fp16 MMA)
+// Whole states run the tcgen05 kernel (kda_fwd_tc.cuh: state in tensor memory,
+// state products on the 5th-generation tensor core); V-row slices run the
+// warp-MMA kernel (kda_fwd_mma.cuh), whose warp roles are:
+//   warp 0        TMA producer: streams the 16-token q/k/v/g tiles of each
+//                 chunk into a 6-deep shared-memory ring.
+//   warps 1..6    three "prep lanes" of two warps each, taking every third
+//                 chunk: gate activation in base 2, in-chunk cumsum, the
+//                 exponent-scaled operand tiles, the 16x16 chunk matrix A and
+//                 the intra-chunk score matrix P (two bf16 warp-MMA products
+//                 per entry), and the unit-lower inverse T = (I + A)^-1 as a
+//                 four-factor Neumann product on fp16 warp MMA.
+//   warps 7..     scan warps, 16 V rows each, holding their rows of the fp32
+//                 state S in registers across the whole sequence. Per chunk:
+//                   Z   = S [K*Gamma ; Q*Gamma]^T              (bf16 MMA)
+//                   R   = V^T - Z_k,  E = R (T diag(beta))^T   (fp16 MMA)
+//                   O   = scale (Z_q + E P^T)                  (fp16 MMA)
+//                   S   = S Diag(gamma) + E Kbar               (fp16 MMA)
 //
 // The chunk algebra follows from unrolling the gated delta rule over a chunk
 // of rows r = 1..L starting from S0: with Gamma_r the in-chunk cumulative
@@ -132,7 +135,7 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    v1::kda_fwd_kernel<NS, QKN><<<static_cast<unsigned>(grid), 32 * (5 + NS), v1::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    v1::kda_fwd_kernel<NS, QKN><<<static_cast<unsigned>(grid), 32 * (1 + 2 * v1::NP + NS), v1::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
 }
 
@@ -350,9 +353,11 @@ KDA_API kda_status kda_decode_ex(const void *q, const void *k, const void *v, co
     p.H = static_cast<int>(H);
     p.scale = scale;
     p.lower_bound = lower_bound;
-    p.qk_norm = (flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
     const int64_t grid = S * H * (DH / dec::ROWS_PER_CTA);
-    dec::kda_decode_kernel<<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    if (flags & KDA_FLAG_QK_L2NORM)
+        dec::kda_decode_kernel<true><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    else
+        dec::kda_decode_kernel<false><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString(e));
     return KDA_OK;

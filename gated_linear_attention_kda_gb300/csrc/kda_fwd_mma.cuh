@@ -10,7 +10,7 @@ namespace v1 {
 
 // ---------------------------------------------------------------- shared memory plan
 constexpr int NR = 6;                 // raw q/k/v/g ring depth (chunks)
-constexpr int NP = 2;                 // prep ring depth = number of prep lanes
+constexpr int NP = 3;                 // prep ring depth = number of prep lanes
 
 constexpr int BZ_LD = 272;            // row pitch (bytes) of 128-wide 16-bit tiles (136 elements)
 constexpr int SM_LD = 48;             // row pitch of 16x16 16-bit tiles (24 elements)
@@ -76,7 +76,7 @@ __device__ __forceinline__ float qk_row_scale64(const uint32_t (&kw)[CHUNK], con
 
 // QKN: L2-normalise the q and k rows in the element-wise pass (KDA_FLAG_QK_L2NORM).
 template <int NS, bool QKN>
-__global__ void __launch_bounds__(32 * (5 + NS), 1)
+__global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
     kda_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
 {
@@ -144,9 +144,9 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
         return;
     }
 
-    if (warp < 5) {
+    if (warp < 1 + 2 * NP) {
         // ------------------------------------------------------------ prep lanes
-        const int ln = (warp - 1) >> 1;            // prep lane 0 or 1
+        const int ln = (warp - 1) >> 1;            // prep lane 0 .. NP - 1
         const int lt = threadIdx.x - 32 - 64 * ln;  // 0..63
         const int lw = lt >> 5;                     // warp within the lane
         const uint32_t bar_id = 1 + ln;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(32 * (5 + NS), 1)
     }
 
     // ---------------------------------------------------------------- scan warps
-    const int sw = warp - 5;
+    const int sw = warp - (1 + 2 * NP);
     const int g = lane >> 2, t = lane & 3;
     const int vr0 = slice * (16 * NS) + 16 * sw;
     const size_t st_base = (static_cast<size_t>(seq) * p.H + h) * (DH * DH);
