@@ -25,8 +25,9 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     syms = declared_symbols()
-    assert {"kda_fwd", "kda_fwd_flat", "kda_fwd_packed", "kda_fwd_host", "kda_check_device_status",
-            "kda_last_error", "kda_plan", "kda_gate_scale", "kda_version"} <= set(syms)
+    assert {"kda_fwd", "kda_fwd_flat", "kda_fwd_packed", "kda_fwd_host", "kda_fwd_ex", "kda_decode",
+            "kda_decode_ex", "kda_check_device_status", "kda_last_error", "kda_plan", "kda_gate_scale",
+            "kda_version"} <= set(syms)
 
 
 def test_library_exports_every_declared_symbol(kda):
