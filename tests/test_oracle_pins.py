@@ -288,6 +288,35 @@ def test_split_call_state_carry():
     np.testing.assert_allclose(s2, s, rtol=1e-12, atol=1e-14)
 
 
+def test_final_state_is_affine_in_the_initial_state_and_segments_compose():
+    """Each token maps S to S A_t + B_t (A_t = Diag(alpha_t)(I - beta_t k_t k_t^T), B_t = beta_t v_t
+    k_t^T), so a segment maps S0 to S0 M + C with M the final state from S0 = I and v = 0 and C the
+    final state from S0 = 0; two segments compose to one call. (The algebra a segment-parallel scan
+    over a long sequence would rest on.)"""
+    K = V = 6
+    T = 50
+    q = rng.standard_normal((1, T, 1, K))
+    k = rng.standard_normal((1, T, 1, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((1, T, 1, V))
+    alpha = rng.uniform(0.6, 1.0, (1, T, 1, K))
+    beta = rng.uniform(0.0, 1.0, (1, T, 1))
+
+    def seg(t0, t1, S0, vv):
+        return oracle.core(q[:, t0:t1], k[:, t0:t1], vv[:, t0:t1], alpha[:, t0:t1], beta[:, t0:t1], 1.0,
+                           initial_state=S0)[1][0, 0]
+
+    eye = np.eye(K)[None, None]
+    zero_v = np.zeros_like(v)
+    M1, C1 = seg(0, 20, eye, zero_v), seg(0, 20, None, v)
+    M2, C2 = seg(20, T, eye, zero_v), seg(20, T, None, v)
+    S0 = rng.standard_normal((1, 1, V, K))
+    _, full = oracle.core(q, k, v, alpha, beta, 1.0, initial_state=S0)
+    np.testing.assert_allclose(S0[0, 0] @ M1 + C1, seg(0, 20, S0, v), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose((S0[0, 0] @ M1 + C1) @ M2 + C2, full[0, 0], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(S0[0, 0] @ (M1 @ M2) + (C1 @ M2 + C2), full[0, 0], rtol=1e-11, atol=1e-12)
+
+
 def test_varlen_equals_separate_calls():
     """Packed sequences with cu_seqlens equal separate per-sequence calls ("Variable-Length Mode")."""
     lens = [5, 37, 16, 1, 23, 0, 40]
