@@ -108,6 +108,23 @@ def test_host_validation_rejects(kda, over, code):
 
 
 
+def test_plain_c_program_uses_the_abi(kda, tmp_path):
+    """A C program built against include/kda.h and linked to libkda.so (no Python, no CUDA
+    headers) runs the host-side parts of the ABI."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = os.path.join(ROOT, "tests", "c_abi_consumer.c")
+    libdir = os.path.dirname(kda.LIB_PATH)
+    exe = str(tmp_path / "c_abi_consumer")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe,
+                    "-L", libdir, "-lkda", f"-Wl,-rpath,{libdir}", "-lm"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.count("ok ") == 11
+
+
 @pytest.mark.parametrize("flags", [2, 4, 0x80000000, 3])
 def test_unknown_option_bits_are_rejected_on_the_host(kda, flags):
     lib = kda.library()
