@@ -251,18 +251,24 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
+    # per-call CUDA events on the launching stream; ms_per_step is the median call, the mean is kept
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_start = time.perf_counter()
     e0.record(stream)
-    for _ in range(args.steps):
+    for a, b in ev:
+        a.record(stream)
         step()
+        b.record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     t_end = time.perf_counter()
     barrier(world)
-    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    per_call = [a.elapsed_time(b) for a, b in ev]
+    median_ms = max_over_ranks(statistics.median(per_call), world)
+    mean_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     clocks = sampler.stop(t_start, t_end) if rank == 0 else None
     kda.check_device_status()
 
@@ -285,12 +291,13 @@ def run_ours(args, world, rank, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "g", "beta"))
     d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+    ceiling = copy_ceiling(h2d, d2h, dev)
 
     if rank != 0:
         return
     tokens = B * T
-    ms_per_step = elapsed_ms / args.steps
-    value = job_throughput(world, tokens, args.steps, elapsed_ms / 1e3)
+    ms_per_step = median_ms
+    value = job_throughput(world, tokens, 1, median_ms / 1e3)
     nbytes, nflops = algorithmic(WORKLOAD, d)
     hbm, tflops, src = peaks()
     achieved = nbytes / (ms_per_step / 1e3) / 1e9
@@ -314,12 +321,36 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic, "peak_source": src, "algorithmic_bytes_per_launch": nbytes,
                      "tensor_frac": (nflops / (ms_per_step / 1e3) / 1e12) / tflops},
         "cpu_baseline": cpu_baseline(d) if world == 1 or rank == 0 else None,
+        "ms_per_step_mean": mean_ms,
         "e2e": {"value": job_throughput(world, tokens, e2e_steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copy_ceiling": dict(ceiling, tokens_per_s=tokens / (h2d / (ceiling["h2d_gbs"] * 1e9)
+                                                                     + d2h / (ceiling["d2h_gbs"] * 1e9)))},
         "clocks": clocks,
         "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
+
+
+def copy_ceiling(h2d, d2h, dev):
+    """Measured pinned-host <-> device copy rates (one cudaMemcpyAsync each way of the step's own
+    byte counts, best of 3): the link's ceiling for the end-to-end number."""
+    import torch
+    res = {}
+    for name, nbytes, to_dev in (("h2d_gbs", h2d, True), ("d2h_gbs", d2h, False)):
+        host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        devb = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        best = float("inf")
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            (devb.copy_(host, non_blocking=True) if to_dev else host.copy_(devb, non_blocking=True))
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        res[name] = nbytes / best / 1e9
+        del host, devb
+    return res
 
 
 def run_launches(n):

@@ -142,7 +142,18 @@ def _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
     S = N if cu_seqlens is not None else B
     for name, t in (("initial_state", initial_state), ("final_state", final_state)):
         _check(name, t, None, (S, H, V, K), cuda)
+    _same_device(q.device, (("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out), ("A_log", A_log),
+                            ("dt_bias", dt_bias), ("initial_state", initial_state), ("final_state", final_state),
+                            ("cu_seqlens", cu_seqlens)))
     return B, T, H, K, V, N
+
+
+def _same_device(dev, named):
+    """Every given tensor must live on ``dev`` (q's device): the library launches on that device
+    and dereferences every pointer there, so a tensor on another GPU is rejected here."""
+    for name, t in named:
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, but q is on {dev}: all tensors must share one device")
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
@@ -225,6 +236,8 @@ def decode(q, k, v, g, beta, scale, out, state, A_log=None, dt_bias=None, lower_
     _check("A_log", A_log, torch.float32, (H,), True)
     _check("dt_bias", dt_bias, torch.float32, (H, K), True)
     _check("state", state, None, (S, H, V, K), True)
+    _same_device(q.device, (("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out), ("A_log", A_log),
+                            ("dt_bias", dt_bias), ("state", state)))
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = _lib.kda_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
@@ -272,10 +285,19 @@ def fwd_host(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound
     return out, final_state
 
 
-def check_device_status(stream=None):
-    """Synchronise ``stream`` and raise if the kernels flagged a device-side error."""
-    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
-    _raise(_lib.kda_check_device_status(ctypes.c_void_p(s)))
+def check_device_status(device=None, stream=None):
+    """Synchronise ``stream`` (default: the current stream of ``device``) and raise if a kernel on
+    that device flagged an error. ``device`` is a ``torch.device``, an index or a tensor (its
+    device); by default the current device. The error word is shared by every call on the device
+    and is read and cleared in one step, so a flag is reported once, by the first check after it."""
+    if isinstance(device, torch.Tensor):
+        device = device.device
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream
+        _raise(_lib.kda_check_device_status(ctypes.c_void_p(s)))
 
 
 def gate_scale(lower_bound: float) -> float:

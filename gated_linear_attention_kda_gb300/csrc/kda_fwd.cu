@@ -170,6 +170,18 @@ static cudaError_t launch_split(int vs, int64_t grid, cudaStream_t s, const CUte
 
 static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Snapshot of the device error word, taken and cleared in one atomic step by status_take_kernel.
+__device__ unsigned int g_dev_error_seen;
+
+__global__ void status_take_kernel() { g_dev_error_seen = atomicExch(&g_dev_error, 0u); }
+
+// An empty call (no tokens): every cu_seqlens entry must be 0, since cu[0] = 0 and cu[N] = B * T = 0.
+__global__ void empty_seqlens_check_kernel(const int64_t *cu, int n)
+{
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        if (cu[i] != 0) atomicOr(&g_dev_error, DEVERR_SEQLENS);
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -244,6 +256,24 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
             return fail(KDA_ERR_RANGE, "KDA_V_SPLIT must be 1, 2, 4 or 8 (got '%s')", env);
     }
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (total == 0) {
+        // No tokens: nothing to launch the forward kernels for. Every sequence is empty, so the
+        // final state is the initial state (or zero); only cu_seqlens is still checked.
+        cudaError_t e = cudaSuccess;
+        if (cu_seqlens) {
+            empty_seqlens_check_kernel<<<1, 256, 0, s>>>(cu_seqlens, static_cast<int>(N + 1));
+            e = cudaGetLastError();
+        }
+        const size_t fin_bytes = static_cast<size_t>(nseq * H) * DH * DH * (final_dtype == KDA_DTYPE_FP32 ? 4 : 2);
+        if (e == cudaSuccess && final_state && initial_state && initial_state != final_state)
+            e = cudaMemcpyAsync(final_state, initial_state, fin_bytes, cudaMemcpyDeviceToDevice, s);
+        else if (e == cudaSuccess && final_state && !initial_state)
+            e = cudaMemsetAsync(final_state, 0, fin_bytes, s);
+        if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "empty call: %s", cudaGetErrorString(e));
+        return KDA_OK;
+    }
+
     CUtensorMap mq, mk, mv, mg, mo;
     std::memset(&mo, 0, sizeof mo);
     std::memset(&mq, 0, sizeof mq);
@@ -284,7 +314,6 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
         grid = nseq * H * vs;
     }
     p.vsplit = vs;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, mo, p)
                                       : launch_split<false>(vs, grid, s, mq, mk, mv, mg, mo, p);
     if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(ce));
@@ -393,11 +422,16 @@ KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, 
 
 KDA_API kda_status kda_check_device_status(void *stream)
 {
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "stream synchronize failed: %s", cudaGetErrorString(e));
-    unsigned int word = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&word, g_dev_error, sizeof word);
-    if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero);
+    t_last_error.clear();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    // one thread exchanges the word with 0 (read and clear in one atomic step, so a bit that a
+    // kernel on another stream sets meanwhile is kept for the next check), then the snapshot is
+    // copied back behind it on the same stream
+    status_take_kernel<<<1, 1, 0, s>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&word, g_dev_error_seen, sizeof word, 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "reading the device status failed: %s", cudaGetErrorString(e));
     if (word)
         return fail(KDA_ERR_DEVICE, "device error word 0x%x:%s%s", word, (word & DEVERR_SEQLENS) ? " bad cu_seqlens" : "",

@@ -119,6 +119,9 @@ typedef enum kda_dtype {
  *   N            number of sequences in varlen mode (>= 1); ignored otherwise.
  *   stream       a cudaStream_t (NULL = legacy default stream).
  * A state absent from the call is zero (initial) or not written (final).
+ * A call with no tokens (B * T == 0) launches no forward kernel: final_state
+ * (if given) receives initial_state, or zeros; in varlen mode every
+ * cu_seqlens entry must then be 0, and a nonzero one flags KDA_ERR_DEVICE.
  * Returns KDA_OK once the work is enqueued. Argument errors are detected on
  * the host before anything is launched and leave every buffer untouched.
  * The environment variable KDA_V_SPLIT (1, 2, 4 or 8), when set, overrides the
@@ -273,10 +276,14 @@ KDA_API kda_status kda_plan(int64_t units, int num_sms, int *v_split, int64_t *g
 KDA_API const char *kda_last_error(void);
 
 /*
- * kda_check_device_status -- synchronises `stream`, then reads and clears the
- * library's device error word (bad cu_seqlens entries, or a pipeline wait
- * that hit its iteration limit). Returns KDA_OK, KDA_ERR_DEVICE (details in
- * kda_last_error()) or KDA_ERR_LAUNCH.
+ * kda_check_device_status -- reads and clears the library's device error
+ * word of the current device (bad cu_seqlens entries, or a pipeline wait that
+ * hit its iteration limit) and synchronises `stream`. The word is shared by
+ * every call of this library on the device: it is exchanged with 0 by one
+ * atomic operation on `stream`, so a flag set by any earlier call is reported
+ * once, by the first check that runs after it, and a flag raised meanwhile by
+ * a kernel on another stream is kept for the next check. Returns KDA_OK,
+ * KDA_ERR_DEVICE (details in kda_last_error()) or KDA_ERR_LAUNCH.
  */
 KDA_API kda_status kda_check_device_status(void *stream);
 

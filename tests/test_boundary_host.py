@@ -183,3 +183,28 @@ def test_python_wrapper_rejects_bad_tensors(kda):
     with pytest.raises(ValueError, match="contiguous"):
         qt = torch.zeros(1, 16, 1, 256, dtype=torch.bfloat16)[..., :128]
         kda.fwd_host(qt, q, q, q, beta, 1.0, q.clone())
+
+
+def test_python_wrapper_rejects_tensors_on_another_device(kda):
+    """Every tensor must live on q's device (the library launches there and dereferences every
+    pointer there). The device check is reached on the host path with a tensor on the `meta`
+    device standing in for a second device; the decode wrapper shares the same check."""
+    import torch
+    q = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16)
+    beta = torch.zeros(1, 16, 1, dtype=torch.bfloat16)
+    other = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16, device="meta")
+    for pos in range(1, 4):
+        args = [q, q, q, q]
+        args[pos] = other
+        with pytest.raises(ValueError, match="all tensors must share one device"):
+            kda.fwd_host(*args, beta, 1.0, q.clone())
+    with pytest.raises(ValueError, match="out is on meta"):
+        kda.fwd_host(q, q, q, q, beta, 1.0, other)
+    with pytest.raises(ValueError, match="beta is on meta"):
+        kda.fwd_host(q, q, q, q, beta.to("meta"), 1.0, q.clone())
+    st = torch.zeros(1, 1, 128, 128, dtype=torch.float32)
+    with pytest.raises(ValueError, match="final_state is on meta"):
+        kda.fwd_host(q, q, q, q, beta, 1.0, q.clone(), initial_state=st, final_state=st.to("meta"))
+    kda._same_device(q.device, (("k", q), ("state", st)))  # same device: accepted
+    with pytest.raises(ValueError, match="state is on meta"):
+        kda._same_device(q.device, (("k", q), ("state", st.to("meta"))))

@@ -155,6 +155,50 @@ def test_bad_cu_seqlens_flags_device_error_without_fault():
     torch.cuda.synchronize()   # the context is still healthy
 
 
+@pytest.mark.parametrize("states", ["none", "initial_only", "final_only", "both", "in_place"])
+def test_empty_call_passes_the_state_through(states):
+    """T = 0: no forward kernel runs; final_state receives initial_state, or zeros without one."""
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("b2_t128_h8", T=0)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    init = c["initial_state"] if states in ("initial_only", "both", "in_place") else None
+    fin = None
+    if states in ("final_only", "both"):
+        fin = torch.full_like(c["initial_state"], float("nan"))
+    elif states == "in_place":
+        fin = init
+    before = None if init is None else init.clone()
+    out = torch.empty_like(c["v"])
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], init, fin)
+    kda.check_device_status()
+    if fin is not None:
+        assert torch.equal(fin, before if before is not None else torch.zeros_like(fin))
+    if init is not None:
+        assert torch.equal(init, before)
+
+
+def test_empty_varlen_call_and_its_cu_seqlens_check():
+    """Varlen with every sequence empty: the bf16 final states equal the initial ones; a nonzero
+    cu_seqlens entry in an empty call is flagged on the device, without a fault."""
+    import gated_linear_attention_kda_gb300 as kda
+    d = W.make("varlen_n16_h32", lengths=[0, 0, 0], H=2)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    out = torch.empty_like(c["v"])
+    fin = torch.full_like(c["initial_state"], float("nan"))
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+    kda.check_device_status()
+    assert torch.equal(fin, c["initial_state"])
+    bad = torch.tensor([0, 5, 5, 5], dtype=torch.int64, device="cuda")
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], fin, bad)
+    with pytest.raises(kda.KDAError, match="KDA_ERR_DEVICE"):
+        kda.check_device_status(bad)
+    kda.check_device_status(bad.device)  # reported once, then cleared
+    torch.cuda.synchronize()
+
+
 def test_host_entry_point_matches_device_entry_point():
     import gated_linear_attention_kda_gb300 as kda
     d = W.make("b2_t128_h8", T=45)
@@ -219,21 +263,55 @@ def test_no_writes_outside_out_and_final_state(H):
 
 # ------------------------------------------------------------ full-size workloads
 
-def test_full_b8_t4096_h16_sampled_heads():
-    """The throughput workload at full size, in the launch configuration the
-    benchmark times; the oracle checks every token of three sampled heads."""
-    d = W.make("b8_t4096_h16")
-    _check(d, heads=[0, 7, 15])
+def _check_every_head(name, final_dtype, group):
+    """A full-size workload in the launch configuration the benchmark times, compared with the
+    oracle on EVERY token of EVERY head. The oracle runs in head groups (heads are independent)
+    to bound host memory; the relative L2 error is accumulated over the whole tensor and the
+    elementwise bound is checked in every group."""
+    import gated_linear_attention_kda_gb300 as kda
+    from tests.kda_harness import ABS, REL, REL_L2
+    d = W.make(name)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    H = d["q"].shape[2]
+    nseq = d["q"].shape[0] if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    out = torch.full_like(c["v"], float("nan"))
+    fin = torch.full((nseq, H, 128, 128), float("nan"), device="cuda",
+                     dtype=torch.float32 if final_dtype == "fp32" else torch.bfloat16)
+    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+    kda.check_device_status()
+    out_h, fin_h = out.cpu(), fin.cpu()
+    del c, out, fin
+    acc = {"out": [0.0, 0.0], "final_state": [0.0, 0.0]}
+    for h0 in range(0, H, group):
+        heads = list(range(h0, min(H, h0 + group)))
+        o_ref, s_ref = run_oracle(d, heads=heads)
+        for key, got_t, ref in (("out", out_h[:, :, heads], o_ref), ("final_state", fin_h[:, heads], s_ref)):
+            got = got_t.float().double().numpy()
+            assert got.shape == ref.shape and np.isfinite(got).all(), key
+            err = got - ref
+            acc[key][0] += float(np.sum(err * err))
+            acc[key][1] += float(np.sum(ref * ref))
+            bad = np.abs(err) > ABS + REL * np.abs(ref)
+            assert not bad.any(), f"{key} heads {heads[0]}..{heads[-1]}: {int(bad.sum())} elements out of bound"
+    for key, (e2, r2) in acc.items():
+        rel = math.sqrt(e2 / r2)
+        assert rel <= REL_L2, f"{key}: relative L2 error {rel:.3e} over all heads"
 
 
-def test_full_varlen_n16_h32_sampled_heads():
-    d = W.make("varlen_n16_h32")
-    _check(d, final_dtype="bf16", heads=[0, 31])
+def test_full_b8_t4096_h16_every_head():
+    """B=8, T=4096, H=16, fp32 final state: all 16 heads of all 8 sequences."""
+    _check_every_head("b8_t4096_h16", "fp32", group=16)
 
 
-def test_full_long_context_sampled_head():
-    d = W.make("b1_t131072_h32")
-    _check(d, heads=[5])
+def test_full_varlen_n16_h32_every_head():
+    """16 packed sequences (66 217 tokens), H=32, bf16 initial and final states: all heads."""
+    _check_every_head("varlen_n16_h32", "bf16", group=8)
+
+
+def test_full_long_context_every_head():
+    """B=1, T=131072, H=32, fp32 initial and final states: all 32 heads."""
+    _check_every_head("b1_t131072_h32", "fp32", group=16)
 
 
 # ------------------------------------------------------------ per-step parity (one chunk)
