@@ -16,7 +16,7 @@ namespace kda {
 __device__ __forceinline__ uint32_t movm_t(uint32_t a)
 {
     uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
 }
 

@@ -141,7 +141,7 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
 
 template <bool QKN>
 static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
-                             const CUtensorMap &v, const CUtensorMap &g, const CUtensorMap &o, const Params &p)
+                             const CUtensorMap &v, const CUtensorMap &g, const Params &p)
 {
     static thread_local int configured_dev = -1;
     int dev = 0;
@@ -152,16 +152,16 @@ static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q,
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    tcs::kda_fwd_tc_kernel<QKN><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, o, p);
+    tcs::kda_fwd_tc_kernel<QKN><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
 }
 
 template <bool QKN>
 static cudaError_t launch_split(int vs, int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
-                                const CUtensorMap &v, const CUtensorMap &g, const CUtensorMap &o, const Params &p)
+                                const CUtensorMap &v, const CUtensorMap &g, const Params &p)
 {
     switch (vs) {
-        case 1: return launch_tc<QKN>(grid, s, q, k, v, g, o, p);
+        case 1: return launch_tc<QKN>(grid, s, q, k, v, g, p);
         case 2: return launch<4, QKN>(grid, s, q, k, v, g, p);
         case 4: return launch<2, QKN>(grid, s, q, k, v, g, p);
         default: return launch<1, QKN>(grid, s, q, k, v, g, p);
@@ -274,15 +274,14 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
         return KDA_OK;
     }
 
-    CUtensorMap mq, mk, mv, mg, mo;
-    std::memset(&mo, 0, sizeof mo);
+    CUtensorMap mq, mk, mv, mg;
     std::memset(&mq, 0, sizeof mq);
     std::memset(&mk, 0, sizeof mk);
     std::memset(&mv, 0, sizeof mv);
     std::memset(&mg, 0, sizeof mg);
     if (total > 0) {
         if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) || !make_map(&mv, v, total, H) ||
-            !make_map(&mg, g, total, H) || !make_map(&mo, out, total, H))
+            !make_map(&mg, g, total, H))
             return fail(KDA_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad geometry)");
     }
     int dev = 0, nsm = 0;
@@ -314,8 +313,8 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
         grid = nseq * H * vs;
     }
     p.vsplit = vs;
-    ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, mo, p)
-                                      : launch_split<false>(vs, grid, s, mq, mk, mv, mg, mo, p);
+    ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, p)
+                                      : launch_split<false>(vs, grid, s, mq, mk, mv, mg, p);
     if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(ce));
     return KDA_OK;
 }

@@ -90,6 +90,32 @@ __device__ __forceinline__ void mma_ts_tf32(uint32_t d, uint32_t a_tmem, uint64_
                  : "memory");
 }
 
+// Warp-wide issue forms: executed by all 32 lanes of a warp together (convergent), the warp
+// elects one lane -- always the lowest, so the same lane every time -- which issues the MMA or the
+// commit. Operands computed by the whole warp stay warp-uniform, so no lane-0 branch is needed.
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+                 "setp.ne.u32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(id), "r"(accumulate)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+                 "setp.ne.u32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+                 : "memory");
+}
+__device__ __forceinline__ void commit_w(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
 // 32 lanes (this warp's quarter) x 32 consecutive 32-bit columns
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
 {

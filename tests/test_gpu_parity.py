@@ -111,6 +111,32 @@ def test_deterministic_repeats(H):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("case", ["lb0", "varlen"])
+def test_ten_repeats_bitwise_identical_and_within_tolerance(case):
+    """The whole-state (tcgen05) kernel ten times on the same inputs: every repeat bitwise equal to
+    the first and within tolerance of the oracle. lower_bound 0 keeps every cross-chunk correction
+    term at full weight; the varlen case mixes ragged sequences in one launch."""
+    if case == "lb0":
+        d = W.make("b2_t128_h8", B=1, T=133, H=80)
+        kw = {"lower_bound": 0.0}
+        fdt = "fp32"
+    else:
+        d = W.make("varlen_n16_h32", lengths=[5, 37, 16, 1, 0, 23, 64, 40, 200, 17], H=12)
+        kw = {}
+        fdt = "bf16"
+    first = run_gpu(d, final_dtype=fdt, **kw)
+    for _ in range(9):
+        again = run_gpu(d, final_dtype=fdt, **kw)
+        assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+    heads = [0, 41, 79] if case == "lb0" else None
+    o_ref, s_ref = run_oracle(d, heads=heads, lower_bound=kw.get("lower_bound"))
+    o, s = first
+    if heads is not None:
+        o, s = o[:, :, heads], s[:, heads]
+    assert_close("out", o, o_ref)
+    assert_close("final_state", s, s_ref)
+
+
 @pytest.mark.parametrize("H", KERNEL_HEADS)
 def test_no_final_state_and_zero_scale(H):
     d = W.make("b1_t64_h1", H=H)
