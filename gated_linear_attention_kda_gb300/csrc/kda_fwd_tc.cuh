@@ -3,37 +3,46 @@
 // per (sequence, head) state, all 128 V rows.
 //
 // Chunk algebra. For chunk n (16 tokens) with state S_n (V x K) at its start,
+// the prep lanes reduce the chunk to
 //   Z_n = [K*Gamma ; Q*Gamma] (32 x K),  Phi_n = [[-T', 0], [-s M, s I]] (32 x 32),
 //   TM_n = [T' ; s M] (32 x 16),  Kbar_n (16 x K),  gamma_n (K),  V_n,
 // with T' = (I + A)^-1 diag(beta), M = P T', s = scale, so that one product
 // gives both the rows written into the state and the outputs:
-//   [E_n | O_n] = D_n = V_n^T TM_n^T + S_n (Phi_n Z_n)^T,
+//   [E_n | O_n] = D_n = V_n^T TM_n^T + S_n Z_n^T Phi_n^T,
 //   S_{n+1} = S_n Diag(gamma_n) + E_n Kbar_n.
-// (W_n = Phi_n Z_n = [-w ; s q^] with w = T' (K*Gamma), q^ = Q*Gamma - M (K*Gamma).)
+// (Phi_n Z_n = [-w ; s q^] with w = T' (K*Gamma), q^ = Q*Gamma - M (K*Gamma).)
 // The state product is formed two chunks ahead from the decayed state two
 // chunks back and corrected by the two rank-16 updates in between (exact in
 // real arithmetic):
-//   S_n W_n^T = Sb_{n-2} W'_n^T + E_{n-2} (Kbar_{n-2} W'_n^T) + E_{n-1} (Kbar_{n-1} W_n^T),
-//   Sb_{n-2} = f16(S_{n-2} Diag(gamma_{n-2})),  W'_n = W_n Diag(gamma_{n-1}).
-// Every term is a 16-bit tcgen05 MMA into the one accumulator D_n, so the
-// tensor core orders them (same accumulator and shape) and no MMA reads
-// another MMA's result. Only the last term depends on the previous chunk, so
-// each chunk's critical path is one 16-deep MMA plus one commit.
+//   S_n Z_n^T = Sb_{n-2} Z'_n^T + E_{n-2} H''_n + E_{n-1} H_n,
+//   Sb_{n-2} = bf16(S_{n-2} Diag(gamma_{n-2})),  Z'_n = Z_n Diag(gamma_{n-1}),
+//   H_n = Kbar_{n-1} Z_n^T,  H''_n = Kbar_{n-2} Diag(gamma_{n-1}) Z_n^T,
+// so D_n = V_n^T TM_n^T + X_n Phi_n^T + E_{n-1} (H_n Phi_n^T), where
+// X_n = Sb_{n-2} Z'_n^T + E_{n-2} H''_n is accumulated in tensor memory and
+// read back as the (tf32) A operand of the Phi product. Only the last term
+// depends on the previous chunk's result, so each chunk's critical path is one
+// 16-deep MMA plus one commit, and the prep lanes never form the 32 x K rows
+// of w and q^ themselves. The slot stores Z' (the prep of chunk n reads
+// gamma_{n-1} from the other lane's slot), so the state warps scale the state
+// by their own chunk's gate only.
 //
-// Warp roles (448 + 64 NFIN threads):
+// Warp roles (512 threads):
 //   warp 0      TMA producer (lane 0); allocates / frees tensor memory.
 //   warp 1      MMA issuer: the whole warp runs the issue loop with warp-uniform
 //               operands and one elected lane issues each MMA and commit.
 //   warps 2-5   state warps, one V row per thread (tensor-memory lane):
 //               read [E|O], hand E to the tensor core, decay the state
-//               (S <- S Diag(gamma)) and keep its f16 copy, store outputs.
+//               (S <- S Diag(gamma)) and keep its bf16 copy, store outputs.
 //   warps 6-13  two prep lanes of four warps, alternate chunks: gate, scaled
-//               key / query tiles, chunk-product partial sums.
-//   warps 14..  NFIN finishers per lane (with two, one per 16-row half of W):
-//               T', M, TM, W = Phi Z (written over Z as W'), Kbar_{n-1} W^T
-//               and Kbar_{n-2} W'^T; they hand the slot to the tensor core.
+//               key / query tiles, chunk-product partial sums, H and H''.
+//   warps 14-15 one finisher per lane: T', M, TM, Phi, (H Phi^T)^T; hands
+//               the slot to the tensor core.
 // Tensor memory (512 columns): state fp32 [0,128), D x3 [128,224),
-// E x2 (f16 pairs) [224,240), f16 state copies x2 [256,384).
+// E x2 (f16 pairs) [224,240), bf16 state copies x2 [256,384), X x2 [384,448).
+// X_n is written by MMAs and then read as the A operand of the tf32 Phi MMAs
+// into a different accumulator; the tensor core orders only MMAs into the same
+// accumulator, so X_n is committed and waited on before it is read, and the two
+// X buffers alternate between chunks.
 //
 // Page references: base-2 gate with the LOG2E-folded scale and the tanh form
 // of the sigmoid ("FlashKDA lower_bound Parameter ..." -- "Conversion to the
@@ -50,57 +59,58 @@ namespace kda {
 namespace tcs {
 
 constexpr int NR = 3;  // raw chunk ring
-// prep slot ring: slot n is last read by the finisher of chunk n + 2 (Kbar_n); with five slots a
-// prep lane refilling a slot waits on the other lane's finisher, never on its own
-constexpr int NP = 5;
-// finisher warps per prep lane (1 or 2)
-constexpr int NFIN = 1;
-constexpr int NTHREADS = 32 * (14 + 2 * NFIN);
-constexpr int W_UNROLL = 1;  // unroll of the finisher's 16-channel loop (code size against overlap)
+constexpr int NP = 4;  // prep slot ring
+constexpr int NTHREADS = 512;
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t T_S = 0;     // fp32 state, 128 columns
 constexpr uint32_t T_D = 128;   // D[3], 32 columns each
 constexpr uint32_t T_E = 224;   // E[2], 8 columns each (16 f16)
-constexpr uint32_t T_SB = 256;  // f16 state copies [2], 64 columns each
+constexpr uint32_t T_SB = 256;  // bf16 state copies [2], 64 columns each
+constexpr uint32_t T_X = 384;   // X[2], 32 fp32 columns each
 
 // prep slot (bytes)
-constexpr int L_Z = 0;         // f16 Z, then W' in place: K-major 128B swizzle, 2 K-blocks x [32 rows][128 B]
+constexpr int L_Z = 0;         // bf16 Z, K-major 128B swizzle: 2 K-blocks x [32 rows][128 B]
 constexpr int L_V16 = 8192;    // f16 V, MN-major 128B swizzle: 2 boxes x [16 rows][128 B]
 constexpr int L_KB = 12288;    // f16 Kbar [16 j][128 c], MN-major 128B swizzle (the raw-tile layout)
-constexpr int L_TM = 16384;    // f16 TM [32 n][16 k]
-constexpr int L_CC = 17408;    // f16 (Kbar_{n-1} W^T)^T [32 n][16 k]
-constexpr int L_HP = 18432;    // f16 (Kbar_{n-2} W'^T)^T [32 n][16 k]
-constexpr int L_GAM = 19456;   // fp32 gamma [128]
-constexpr int SLOT = 20480;
+constexpr int L_PHI = 16384;   // fp32 Phi [32 n][32 k], K-major core matrices (LBO 128, SBO 1024)
+constexpr int L_TM = 20480;    // f16 TM [32 n][16 k]
+constexpr int L_CC = 21504;    // f16 (H Phi^T)^T [32 n][16 k]
+constexpr int L_HP = 22528;    // f16 H''^T [32 n][16 k]
+constexpr int L_GAM = 23552;   // fp32 gamma [128]
+constexpr int SLOT = 24576;
 
-// prep scratch (per lane); fp32 tiles are [16][132] (528-byte rows: ldmatrix rows fall in distinct banks)
-constexpr int F_LD = 528;
-constexpr int S_KL = 0;                  // fp32 K * 2^(G - G_mid)
-constexpr int S_QL = S_KL + 16 * F_LD;   // fp32 Q * 2^(G - G_mid)
-constexpr int S_KR = S_QL + 16 * F_LD;   // fp32 K * 2^(G_mid - G)
+// prep scratch (per lane); 16-bit tiles are [16][136] (272-byte rows)
+constexpr int H_LD = 272;
+constexpr int S_KLH = 0;                 // bf16 K * 2^(G - G_mid)
+constexpr int S_QLH = S_KLH + 16 * H_LD; // bf16 Q * 2^(G - G_mid)
+constexpr int S_KRH = S_QLH + 16 * H_LD; // bf16 hi / lo of K * 2^(G_mid - G)
+constexpr int S_KRL = S_KRH + 16 * H_LD;
+constexpr int S_KG = S_KRL + 16 * H_LD;  // f16 K * Gamma
+constexpr int S_QG = S_KG + 16 * H_LD;   // f16 Q * Gamma
 // handed to the lane's finisher warp, two buffers (alternate chunks of the lane)
-constexpr int S_BETA = S_KR + 16 * F_LD; // fp32 [2][16] beta
-constexpr int S_GP = S_BETA + 128;        // fp32 [2][4 warps][2 tiles][32 lanes][4]: A (warps 0, 2) and P (1, 3) partial
-                                          // sums; before them the chunk's gate sums [4 row quarters][32 lanes][4]
-constexpr int SCR = S_GP + 2 * 4096;
+constexpr int S_BETA = S_QG + 16 * H_LD; // fp32 [2][16] beta
+constexpr int S_GP = S_BETA + 128;       // fp32 [2][4 warps][2 tiles][32 lanes][4]: A (warps 0, 2) and P (1, 3) partial
+                                         // sums; before them the chunk's gate sums [4 row quarters][32 lanes][4]
+constexpr int S_HX = S_GP + 2 * 4096;    // [2][H^w as an f16 A fragment (32 lanes x 16 B) | H^q fragments (2 x 32 lanes x 16 B)]
+constexpr int SCR = S_HX + 2 * 1536;
 
 constexpr int OFF_RAW = 0;
 constexpr int OFF_SLOT = OFF_RAW + NR * RAW_STAGE;
 constexpr int OFF_SCR = OFF_SLOT + NP * SLOT;
 constexpr int OFF_BAR = OFF_SCR + 2 * SCR;
 // barrier indices
-constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = B_RAW_FULL + NR, B_PREP_FULL = B_RAW_EMPTY + NR,
-              B_PREP_EMPTY = B_PREP_FULL + NP, B_P2 = B_PREP_EMPTY + NP, B_D = B_P2 + NP, B_E = B_D + 2, B_G = B_E + 2,
-              B_S = B_G + 2, B_I = B_S + 2, B_F = B_I + 1, B_GRAM = B_F + 1, B_FDONE = B_GRAM + 4, B_ZREAD = B_FDONE + 4,
-              NBARS = B_ZREAD + 4;
+constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = 4, B_PREP_FULL = 8, B_PREP_EMPTY = 12, B_D = 16, B_E = 18, B_G = 20,
+              B_S = 22, B_I = 24, B_F = 25, B_P2 = 26, B_GRAM = 30, B_HRDY = 34, B_FDONE = 38, B_GAM = 42, B_X = 46,
+              NBARS = 48;
 constexpr int OFF_TMEMPTR = OFF_BAR + NBARS * 8;
 constexpr int OFF_FLAGS = OFF_TMEMPTR + 16;
 constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;
 
+static_assert(NR <= 4 && NP == 4, "barrier index ranges");
 static_assert(SLOT % 1024 == 0 && OFF_SLOT % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled operands need 1024-byte alignment");
-static_assert(S_BETA % 16 == 0 && S_GP % 16 == 0 && SCR % 16 == 0, "alignment");
+static_assert(S_KG % 16 == 0 && S_GP % 16 == 0 && S_HX % 16 == 0 && SCR % 16 == 0, "alignment");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -110,7 +120,13 @@ __device__ __forceinline__ uint32_t cm16(int n, int k)
 {
     return (n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
 }
-// byte offset of (row, col) in a 16-bit K-major 128B-swizzled operand, K = 128
+// byte offset of (row n, col k) in a K-major, non-swizzled fp32 (tf32) operand
+// with 32 K elements per row: 8 x 4 core matrices, LBO = 128 (K), SBO = 1024 (N)
+__device__ __forceinline__ uint32_t cm32(int n, int k)
+{
+    return (n >> 3) * 1024 + (k >> 2) * 128 + (n & 7) * 16 + (k & 3) * 4;
+}
+// byte offset of (row, col) in a bf16 K-major 128B-swizzled operand, K = 128
 // as two 64-column blocks of 32 rows
 __device__ __forceinline__ uint32_t sw128_32rows(int row, int c)
 {
@@ -118,21 +134,37 @@ __device__ __forceinline__ uint32_t sw128_32rows(int row, int c)
 }
 __device__ __forceinline__ float h_lo(uint32_t w) { return __low2float(*reinterpret_cast<const __half2 *>(&w)); }
 __device__ __forceinline__ float h_hi(uint32_t w) { return __high2float(*reinterpret_cast<const __half2 *>(&w)); }
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
 
-// D_n = V_n^T TM_n^T + Sb[b] W'_n^T [+ E[e] (Kbar_{n-2} W'_n^T)] for the prep slot at `sl`.
-// Executed by the whole issuing warp; one elected lane issues.
-__device__ __forceinline__ void issue_d(uint32_t tmem, uint32_t sl, int dbuf, int b, int e)
+// First half of D_n for the prep slot at `sl`: D_n = V_n^T TM_n^T, and X[xb] = Sb[b] Z'_n^T
+// [+ E[e] H''_n]. Executed by the whole issuing warp; one elected lane issues.
+__device__ __forceinline__ void issue_x(uint32_t tmem, uint32_t sl, int dbuf, int b, int e, int xb)
 {
     const uint32_t id_u = tc::idesc(tc::F16, 128, 32, 1, 0);
     const uint32_t id_c = tc::idesc(tc::F16, 128, 32, 0, 0);
-    const uint32_t dn = tmem + T_D + 32 * dbuf;
-    // descriptor of W', advanced by adding (byte offset >> 4) to the address field
+    const uint32_t id_y = tc::idesc(tc::BF16, 128, 32, 0, 0);
+    const uint32_t dn = tmem + T_D + 32 * dbuf, x = tmem + T_X + 32 * xb;
+    // descriptors of the slot's operands, advanced by adding (byte offset >> 4) to the address field
     const uint64_t dz = tc::sdesc(sl + L_Z, 16, 1024, tc::SWZ_128B);
     tc::mma_ss_w(dn, tc::sdesc(sl + L_V16, 2048, 1024, tc::SWZ_128B), tc::sdesc(sl + L_TM, 128, 256, tc::SWZ_NONE), id_u, 0);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        tc::mma_ts_w(dn, tmem + T_SB + 64 * b + 8 * i, dz + (((i >> 2) * 4096 + (i & 3) * 32) >> 4), id_c, 1);
-    if (e >= 0) tc::mma_ts_w(dn, tmem + T_E + 8 * e, tc::sdesc(sl + L_HP, 128, 256, tc::SWZ_NONE), id_c, 1);
+        tc::mma_ts_w(x, tmem + T_SB + 64 * b + 8 * i, dz + (((i >> 2) * 4096 + (i & 3) * 32) >> 4), id_y, i > 0);
+    if (e >= 0) tc::mma_ts_w(x, tmem + T_E + 8 * e, tc::sdesc(sl + L_HP, 128, 256, tc::SWZ_NONE), id_c, 1);
+}
+
+// Second half, once X[xb] is complete: D_n += X[xb] Phi_n^T (tf32, X as the A operand).
+__device__ __forceinline__ void issue_phi(uint32_t tmem, uint32_t sl, int dbuf, int xb)
+{
+    const uint32_t id_p = tc::idesc(tc::TF32, 128, 32, 0, 0);
+    const uint32_t dn = tmem + T_D + 32 * dbuf, x = tmem + T_X + 32 * xb;
+    const uint64_t dp = tc::sdesc(sl + L_PHI, 128, 1024, tc::SWZ_NONE);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tc::mma_ts_tf32_w(dn, x + 8 * i, dp + ((256 * i) >> 4), id_p, 1);
 }
 
 // L2 scale factors 1 / sqrt(sum x^2 + 1e-6) of the four k rows and four q rows held by this
@@ -166,25 +198,6 @@ __device__ __forceinline__ void qk_row_scales(const uint2 (&kw)[4], const uint2 
     for (int i = 0; i < 4; ++i) {
         sk[i] = __shfl_sync(0xffffffffu, f, 4 * i);
         sq[i] = __shfl_sync(0xffffffffu, f, 16 + 4 * i);
-    }
-}
-
-// acc[nt] (16 rows r x 16 columns j) = sum_c X[r][c] R[j][c] over the 64 channels c in [cbase, cbase + 64),
-// from fp32 tiles [16][132] (528-byte rows), on m16n8k8 tf32 warp MMA. ldmatrix on 32-bit data hands
-// thread 4 g + t the word (row g, column t) of each 8 x 4 block: the tf32 A and B fragment layouts.
-__device__ __forceinline__ void chunk_gram_tf32(uint32_t x, uint32_t r, Frag16 &acc, int lane, int cbase)
-{
-    const int mi = lane >> 3, ri = lane & 7;
-    const uint32_t aoff = (ri + 8 * (mi & 1)) * F_LD + 16 * (mi >> 1) + 4 * cbase;  // A: rows r, k = c
-    const uint32_t boff = (ri + 8 * (mi >> 1)) * F_LD + 16 * (mi & 1) + 4 * cbase;  // B: rows j, k = c
-    frag_zero(acc);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a[4], b[4];
-        ldsm_x4(x + aoff + 32 * kk, a[0], a[1], a[2], a[3]);
-        ldsm_x4(r + boff + 32 * kk, b[0], b[1], b[2], b[3]);
-        mma_tf32(acc.c[0], a, b[0], b[1]);
-        mma_tf32(acc.c[1], a, b[2], b[3]);
     }
 }
 
@@ -226,9 +239,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(B_RAW_EMPTY + i), 1);
         }
         for (int i = 0; i < NP; ++i) {
-            mbar_init(bar(B_PREP_FULL + i), NFIN);           // the chunk's finisher warps
-            mbar_init(bar(B_PREP_EMPTY + i), 1 + 2 * NFIN);  // the state update's commit + the finishers of the next two chunks
-            mbar_init(bar(B_P2 + i), 1);
+            mbar_init(bar(B_PREP_FULL + i), 1);
+            mbar_init(bar(B_PREP_EMPTY + i), 1 + 4);  // the state update's commit + the lane's warps reading it two chunks later
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_D + i), 1);
@@ -238,10 +250,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mbar_init(bar(B_I), 4);
         mbar_init(bar(B_F), 1);
+        mbar_init(bar(B_X + 0), 1);
+        mbar_init(bar(B_X + 1), 1);
         for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(B_P2 + i), 1);
+            mbar_init(bar(B_GAM + i), 1);
             mbar_init(bar(B_GRAM + i), 4);
-            mbar_init(bar(B_FDONE + i), NFIN);
-            mbar_init(bar(B_ZREAD + i), 1);
+            mbar_init(bar(B_HRDY + i), 4);
+            mbar_init(bar(B_FDONE + i), 1);
         }
         flags[0] = 0;
         fence_mbar_init();
@@ -287,20 +303,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 return ok;
             };
+            // D_n for slot n, from the state copy b and (e >= 0) the correction E[e] H''_n: X_n is
+            // committed and waited on before the Phi MMAs read it
+            auto issue_d = [&](int n, int b, int e) {
+                const int xb = n & 1;
+                issue_x(tmem, slot(n), n % 3, b, e, xb);
+                tc::commit_w(bar(B_X + xb));
+                if (!wait_all(B_X + xb, (n >> 1) & 1)) return false;
+                tc::fence_after();
+                issue_phi(tmem, slot(n), n % 3, xb);
+                return true;
+            };
             bool ok = wait_all(B_I, 0);
             for (int n = 0; ok && n < (nch < 2 ? nch : 2); ++n) {
                 ok = wait_all(B_PREP_FULL + n % NP, (n / NP) & 1);
                 if (!ok) break;
                 tc::fence_after();
-                issue_d(tmem, slot(n), n % 3, n & 1, -1);
-                if (n == 0) tc::commit_w(bar(B_D + 0));
+                ok = issue_d(n, n & 1, -1);
+                if (ok && n == 0) tc::commit_w(bar(B_D + 0));
             }
             for (int k = 0; ok && k < nch; ++k) {
                 ok = wait_all(B_E + (k & 1), (k >> 1) & 1);
                 if (!ok) break;
                 tc::fence_after();
                 const uint32_t e = tmem + T_E + 8 * (k & 1);
-                if (k + 1 < nch) {  // D_{k+1} += E_k (Kbar_k W_{k+1}^T)
+                if (k + 1 < nch) {  // D_{k+1} += E_k (H_{k+1} Phi_{k+1}^T)
                     tc::mma_ts_w(tmem + T_D + 32 * ((k + 1) % 3), e, tc::sdesc(slot(k + 1) + L_CC, 128, 256, tc::SWZ_NONE),
                                  id_c, 1);
                     tc::commit_w(bar(B_D + ((k + 1) & 1)));
@@ -317,7 +344,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ok = wait_all(B_PREP_FULL + n % NP, (n / NP) & 1);
                     if (!ok) break;
                     tc::fence_after();
-                    issue_d(tmem, slot(n), n % 3, k & 1, k & 1);
+                    ok = issue_d(n, k & 1, k & 1);
                 }
             }
             tc::commit_w(bar(B_F));
@@ -330,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int row = 32 * q4 + lane;
         const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const size_t st_row = (static_cast<size_t>(seq) * p.H + h) * (DH * DH) + static_cast<size_t>(row) * DH;
-        // S_0, and f16(S_0) for the products of chunks 0 and 1 (chunk 1's W' carries gamma_0)
+        // S_0, and bf16(S_0) for the products of chunks 0 and 1 (chunk 1's Z carries gamma_0)
         bool ok = true;
 #pragma unroll 1
         for (int g4 = 0; g4 < 4; ++g4) {
@@ -364,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) r16[i / 2] = pack_f16(__uint_as_float(r32[i]), __uint_as_float(r32[i + 1]));
+            for (int i = 0; i < 32; i += 2) r16[i / 2] = pack_bf16(__uint_as_float(r32[i]), __uint_as_float(r32[i + 1]));
             tc::st32(lb + T_S + 32 * g4, r32);
             tc::st16(lb + T_SB + 16 * g4, r16);
             tc::st16(lb + T_SB + 64 + 16 * g4, r16);
@@ -399,8 +426,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_E + (k & 1)));
             }
-            // decay the state for this chunk, S <- S Diag(gamma_k), and keep f16 of it for
-            // chunk k + 2's product (whose W' carries gamma_{k+1})
+            // decay the state for this chunk, S <- S Diag(gamma_k), and keep bf16 of it for
+            // chunk k + 2's product (whose Z carries gamma_{k+1})
             ok = (k == 0) || wait_bar(bar(B_S + ((k - 1) & 1)), ((k - 1) >> 1) & 1, flags);
             ok = ok && wait_bar(bar(B_PREP_FULL + k % NP), (k / NP) & 1, flags);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -409,11 +436,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tc::fence_after();
             const uint32_t gam = slot(k) + L_GAM;
-#pragma unroll 1
-            for (int g4 = 0; g4 < 4; ++g4) {
-                uint32_t r32[32], r16[16];
-                tc::ld32(lb + T_S + 32 * g4, r32);
-                tc::wait_ld();
+            auto decay_block = [&](int g4, uint32_t(&r32)[32]) {
+                uint32_t r16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 gv = SM_AT(const float4, gam + (32 * g4 + i) * 4);
@@ -423,11 +447,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     r32[i + 1] = __float_as_uint(a01.y);
                     r32[i + 2] = __float_as_uint(a23.x);
                     r32[i + 3] = __float_as_uint(a23.y);
-                    r16[i / 2] = pack_f16(a01.x, a01.y);
-                    r16[i / 2 + 1] = pack_f16(a23.x, a23.y);
+                    r16[i / 2] = pack_bf16(a01.x, a01.y);
+                    r16[i / 2 + 1] = pack_bf16(a23.x, a23.y);
                 }
                 tc::st32(lb + T_S + 32 * g4, r32);
                 tc::st16(lb + T_SB + 64 * (k & 1) + 16 * g4, r16);
+            };
+#pragma unroll 1
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint32_t ra[32];
+                tc::ld32(lb + T_S + 32 * g4, ra);
+                tc::wait_ld();
+                decay_block(g4, ra);
             }
             tc::wait_st();
             tc::fence_before();
@@ -477,8 +508,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---------------------------------------------------------------- prep lanes
         // lane = 4 warps = 128 threads, alternate chunks. Element-wise passes: thread ->
         // channels [c0, c0 + 4) (c0 = 4 lane), rows [4 rq, 4 rq + 4) (row quarter rq = warp
-        // in lane). The lane forms the gate, the scaled key / query tiles and the
-        // chunk-product partial sums; its finisher warp does the rest.
+        // in lane). The lane forms the gate, the scaled key / query tiles, the chunk-product
+        // partial sums and the cross-chunk products; its finisher warp does the rest.
         const int ln = (warp - 6) >> 2;
         const int lt = threadIdx.x - 192 - 128 * ln;  // 0..127
         const int lw = lt >> 5;
@@ -494,6 +525,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int j = 0; j < 4; ++j) bb[j] = ah2 * __ldg(p.dt_bias + h * DH + c0 + j);
         }
         const float hs = p.half_gs;
+        const int t = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+        // B operand (n = tile row, k = tile column) of a row-major [16][136] 16-bit tile
+        const uint32_t b_row = (ri + 8 * (mi >> 1)) * H_LD + 16 * (mi & 1);
+        // transposed fragment stores into a [32 n][16 k] K-major core-matrix tile: lane 8 mi + ri
+        // addresses row ri of the core matrix (n block mi >> 1, k block mi & 1)
+        const uint32_t stsm_row = (mi >> 1) * 256 + (mi & 1) * 128 + ri * 16;
 
         // bf16 bits of the beta logit of row lt of chunk n, loaded one lane-chunk ahead and
         // left untouched until used (rows past the sequence end read its last row and are
@@ -565,9 +603,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     gr[j] = ex2_approx(gm);            // 2^Gm
                     se[j] = ex2_approx(ge[j] - gm);    // 2^(Ge - Gm)
                 }
-                if (rq == 3)
+                if (rq == 3) {
                     SM_AT(float4, sl + L_GAM + c0 * 4) =
                         make_float4(ex2_approx(ge[0]), ex2_approx(ge[1]), ex2_approx(ge[2]), ex2_approx(ge[3]));
+                    __syncwarp();  // the warp's stores happen before its one arrival
+                    if (lane == 0) mbar_arrive(bar(B_GAM + n % NP));
+                }
+            }
+            // gamma_{n-1} of this thread's channels (the previous chunk, the other lane): the state
+            // product of chunk n reads Z_n Diag(gamma_{n-1}) against the state decayed to the start
+            // of chunk n-1, so Z is stored pre-scaled (gamma_{-1} = 1)
+            float gp[4] = {1.f, 1.f, 1.f, 1.f};
+            if (n >= 1) {
+                if (!wait_bar(bar(B_GAM + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+                const float4 gv = SM_AT(const float4, slot(n + NP - 1) + L_GAM + c0 * 4);
+                gp[0] = gv.x; gp[1] = gv.y; gp[2] = gv.z; gp[3] = gv.w;
             }
             // all raw loads first: stores below may alias them as far as the compiler knows
             uint2 kwv[4], qwv[4], vwv[4];
@@ -605,45 +655,103 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     qg[j] = ql[j] * gr[j];  // Q * Gamma
                     kb[j] = kr[j] * se[j];  // Kbar = K * 2^(Ge - G_r)
                 }
-                const uint32_t o = r * F_LD + c0 * 4;
-                SM_AT(uint2, sl + L_Z + sw128_32rows(r, c0)) = make_uint2(pack_f16(kg[0], kg[1]), pack_f16(kg[2], kg[3]));
-                SM_AT(uint2, sl + L_Z + sw128_32rows(16 + r, c0)) = make_uint2(pack_f16(qg[0], qg[1]), pack_f16(qg[2], qg[3]));
+                const uint32_t o = r * H_LD + c0 * 2;
+                SM_AT(uint2, scr + S_KG + o) = make_uint2(pack_f16(kg[0], kg[1]), pack_f16(kg[2], kg[3]));
+                SM_AT(uint2, scr + S_QG + o) = make_uint2(pack_f16(qg[0], qg[1]), pack_f16(qg[2], qg[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(r, c0)) =
+                    make_uint2(pack_bf16(kg[0] * gp[0], kg[1] * gp[1]), pack_bf16(kg[2] * gp[2], kg[3] * gp[3]));
+                SM_AT(uint2, sl + L_Z + sw128_32rows(16 + r, c0)) =
+                    make_uint2(pack_bf16(qg[0] * gp[0], qg[1] * gp[1]), pack_bf16(qg[2] * gp[2], qg[3] * gp[3]));
                 const uint2 vw = vwv[i];
                 SM_AT(uint2, sl + L_V16 + raw_off(r, c0)) = make_uint2(pack_f16(bf16_lo(vw.x), bf16_hi(vw.x)),
                                                                        pack_f16(bf16_lo(vw.y), bf16_hi(vw.y)));
                 SM_AT(uint2, sl + L_KB + raw_off(r, c0)) = make_uint2(pack_f16(kb[0], kb[1]), pack_f16(kb[2], kb[3]));
-                SM_AT(float4, scr + S_KL + o) = make_float4(kl[0], kl[1], kl[2], kl[3]);
-                SM_AT(float4, scr + S_QL + o) = make_float4(ql[0], ql[1], ql[2], ql[3]);
-                SM_AT(float4, scr + S_KR + o) = make_float4(kr[0], kr[1], kr[2], kr[3]);
+                SM_AT(uint2, scr + S_KLH + o) = make_uint2(pack_bf16(kl[0], kl[1]), pack_bf16(kl[2], kl[3]));
+                SM_AT(uint2, scr + S_QLH + o) = make_uint2(pack_bf16(ql[0], ql[1]), pack_bf16(ql[2], ql[3]));
+                uint32_t h0, l0, h1, l1;
+                split_bf16_trunc(kr[0], kr[1], h0, l0);
+                split_bf16_trunc(kr[2], kr[3], h1, l1);
+                SM_AT(uint2, scr + S_KRH + o) = make_uint2(h0, h1);
+                SM_AT(uint2, scr + S_KRL + o) = make_uint2(l0, l1);
             }
-            tc::fence_async_smem();  // V and Kbar are read by the tensor core
+            tc::fence_async_smem();  // Z', V and Kbar are read by the tensor core
             named_bar_sync(bar_id, 128);
             if (lt == 0) {
                 mbar_arrive(bar(B_RAW_EMPTY + rs));
                 mbar_arrive(bar(B_P2 + n % NP));  // Kbar_n and gamma_n are in the slot
             }
 
-            // A (warps 0, 2) and P (warps 1, 3) partial sums over one channel half each, on tf32 warp MMA
+            // A (warps 0, 2) and P (warps 1, 3) partial sums over one channel half each;
+            // two bf16 products per entry: Kl, Ql rounded once, Kr as hi + lo
             {
                 Frag16 acc;
-                chunk_gram_tf32(scr + ((lw & 1) ? S_QL : S_KL), scr + S_KR, acc, lane, 64 * (lw >> 1));
+                chunk_gram_x2<4>(scr + ((lw & 1) ? S_QLH : S_KLH), scr + S_KRH, scr + S_KRL, acc, lane, 4 * (lw >> 1));
                 const uint32_t gp = scr + S_GP + xb * 4096 + lw * 1024 + lane * 16;
                 SM_AT(float4, gp) = make_float4(acc.c[0][0], acc.c[0][1], acc.c[0][2], acc.c[0][3]);
                 SM_AT(float4, gp + 512) = make_float4(acc.c[1][0], acc.c[1][1], acc.c[1][2], acc.c[1][3]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_GRAM + 2 * ln + xb));
             }
+
+            // cross-chunk products, one per warp (slots n-1, n-2; for n < 2 they read stale
+            // slots and are stored but never used):
+            //   warp 0: H^w = Kbar_{n-1} (K Gamma)^T,   warp 1: H^q = Kbar_{n-1} (Q Gamma)^T,
+            //   warps 2, 3: H'' = Kbar_{n-2} Diag(gamma_{n-1}) [K Gamma ; Q Gamma]^T, one half each
+            if (n >= 1 && !wait_bar(bar(B_P2 + (n - 1) % NP), ((n - 1) / NP) & 1, flags)) failed = true;
+            {
+                const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
+                const uint32_t zt = scr + ((lw & 1) ? S_QG : S_KG) + b_row;
+                const uint32_t hx = scr + S_HX + xb * 1536;
+                float hc[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) hc[i][0] = hc[i][1] = hc[i][2] = hc[i][3] = 0.f;
+                if (lw < 2) {
+#pragma unroll
+                    for (int kb = 0; kb < 8; ++kb) {
+                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));  // A rows j, k = c
+                        uint32_t aK[4], bz[4];
+                        ldsm_x4(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
+                        mma_f16(hc[0], aK, bz[0], bz[1]);
+                        mma_f16(hc[1], aK, bz[2], bz[3]);
+                    }
+                    if (lw == 0) {
+                        SM_AT(uint4, hx + lane * 16) = make_uint4(pack_f16(hc[0][0], hc[0][1]), pack_f16(hc[0][2], hc[0][3]),
+                                                                  pack_f16(hc[1][0], hc[1][1]), pack_f16(hc[1][2], hc[1][3]));
+                    } else {
+                        SM_AT(float4, hx + 512 + lane * 16) = make_float4(hc[0][0], hc[0][1], hc[0][2], hc[0][3]);
+                        SM_AT(float4, hx + 1024 + lane * 16) = make_float4(hc[1][0], hc[1][1], hc[1][2], hc[1][3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int kb = 0; kb < 8; ++kb) {
+                        const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kb + 8 * (mi >> 1));
+                        uint32_t aK[4], bz[4];
+                        ldsm_x4(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
+                        ldsm_x4(zt + 32 * kb, bz[0], bz[1], bz[2], bz[3]);
+                        const float2 gl = SM_AT(const float2, prev + L_GAM + (16 * kb + 2 * t) * 4);
+                        const float2 gh = SM_AT(const float2, prev + L_GAM + (16 * kb + 8 + 2 * t) * 4);
+                        const uint32_t gk0 = pack_f16(gl.x, gl.y), gk1 = pack_f16(gh.x, gh.y);
+                        mma_f16(hc[0], aK, hmul2(bz[0], gk0), hmul2(bz[1], gk1));
+                        mma_f16(hc[1], aK, hmul2(bz[2], gk0), hmul2(bz[3], gk1));
+                    }
+                    // H''^T rows n = Z row (16 per warp), columns k = j
+                    stsm_x4_t(sl + L_HP + (lw == 2 ? 0 : 512) + stsm_row, pack_f16(hc[0][0], hc[0][1]),
+                              pack_f16(hc[0][2], hc[0][3]), pack_f16(hc[1][0], hc[1][1]), pack_f16(hc[1][2], hc[1][3]));
+                    tc::fence_async_smem();  // H''^T is read by the tensor core
+                }
+            }
+            __syncwarp();  // one arrival per warp, after all its lanes' stores and reads
+            if (lane == 0) {
+                mbar_arrive(bar(B_HRDY + 2 * ln + xb));
+                if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));  // last read of slot n - 2
+            }
         }
     } else {
         // ---------------------------------------------------------------- finishers
-        // NFIN warps per prep lane. A and P from the lane's partial sums, T' = (I + A)^-1 diag(beta)
-        // and M = P T'; then, 16 channels at a time, the 16-row halves of W = Phi Z (half 0:
-        // -T' (K Gamma); half 1: s (Q Gamma) - s M (K Gamma)) are written over Z as
-        // W' = W Diag(gamma_{n-1}), and their columns of Kbar_{n-1} W^T and Kbar_{n-2} W'^T are
-        // accumulated; then the slot is handed on. Half 0 writes over the K Gamma rows that half 1
-        // reads: with two warps it stores only once half 1 is done, with one warp it runs second.
-        const int fw = warp - (NTHREADS / 32 - 2 * NFIN);
-        const int ln = fw / NFIN, myhalf = fw % NFIN;
+        // one warp per prep lane: A and P from the lane's partial sums, T' = (I + A)^-1 diag(beta),
+        // M = P T', the TM and Phi operands and (H Phi^T)^T, then the slot is handed on.
+        const int ln = warp - 14;
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
         const float sc = p.scale;
         const int g = lane >> 2, t = lane & 3;
@@ -654,7 +762,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int xb = (n >> 1) & 1;
             const uint32_t xpar = static_cast<uint32_t>(n >> 2) & 1;
             const uint32_t sl = slot(n);
-            const uint32_t gp = scr + S_GP + xb * 4096 + lane * 16;
+            const uint32_t gp = scr + S_GP + xb * 4096 + lane * 16, hx = scr + S_HX + xb * 1536;
             const uint32_t bet = scr + S_BETA + xb * 64;
             if (!__all_sync(0xffffffffu, wait_bar(bar(B_GRAM + 2 * ln + xb), xpar, flags))) break;
             // A = strictly-lower part with rows scaled by beta; P = lower part (diagonal included)
@@ -682,7 +790,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             Frag16 T;
             unit_lower_inverse(A, T, g, t);
             // T' = T diag(beta) rounded to f16 once: tw[col block][row block] in fragment layout;
-            // TM rows 0..15 = T'
+            // TM rows 0..15 = T', Phi rows 0..15 = [-T', 0]
             uint32_t tw[2][2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -690,18 +798,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float2 bc = SM_AT(const float2, bet + col * 4);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
+                    const int r = g + 8 * hh;
                     const uint32_t w = pack_f16(T.c[nt][2 * hh] * bc.x, T.c[nt][2 * hh + 1] * bc.y);
                     tw[nt][hh] = w;
-                    if (myhalf == 0) SM_AT(uint32_t, sl + L_TM + cm16(g + 8 * hh, col)) = w;
+                    SM_AT(uint32_t, sl + L_TM + cm16(r, col)) = w;
+                    SM_AT(float2, sl + L_PHI + cm32(r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                    SM_AT(float2, sl + L_PHI + cm32(r, 16 + col)) = make_float2(0.f, 0.f);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_FDONE + 2 * ln + xb));  // partial sums and beta are read
-            // A fragments of the rows of Phi in the K Gamma columns: -T' (half 0) and -s M (half 1),
-            // M = P T' with s M rounded to f16 once (TM rows 16..31)
-            const uint32_t aT[4] = {tw[0][0] ^ NEG2, tw[0][1] ^ NEG2, tw[1][0] ^ NEG2, tw[1][1] ^ NEG2};
-            uint32_t aM[4] = {0u, 0u, 0u, 0u};
-            if (NFIN == 1 || myhalf == 1) {
+            // M = P T' (B operand: transposed 8x8 blocks of T'); s M rounded to f16 once, shared by
+            // TM rows 16..31, Phi rows 16..31 = [-s M, s I] and the correction
+            uint32_t sm16[2][2];
+            {
                 uint32_t aP[4];
                 frag_as_a(P, aP);
                 float m[2][4];
@@ -710,140 +818,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     m[nb][0] = m[nb][1] = m[nb][2] = m[nb][3] = 0.f;
                     mma_f16(m[nb], aP, movm_t(tw[nb][0]), movm_t(tw[nb][1]));
                 }
-                uint32_t sm16[2][2];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
+                        const int r = g + 8 * hh, col = 8 * nt + 2 * t;
                         const uint32_t w = pack_f16(sc * m[nt][2 * hh], sc * m[nt][2 * hh + 1]);
                         sm16[nt][hh] = w;
-                        SM_AT(uint32_t, sl + L_TM + cm16(16 + g + 8 * hh, 8 * nt + 2 * t)) = w;
+                        SM_AT(uint32_t, sl + L_TM + cm16(16 + r, col)) = w;
+                        SM_AT(float2, sl + L_PHI + cm32(16 + r, col)) = make_float2(-h_lo(w), -h_hi(w));
+                        SM_AT(float2, sl + L_PHI + cm32(16 + r, 16 + col)) = make_float2(r == col ? sc : 0.f, r == col + 1 ? sc : 0.f);
                     }
-                aM[0] = sm16[0][0] ^ NEG2;
-                aM[1] = sm16[0][1] ^ NEG2;
-                aM[2] = sm16[1][0] ^ NEG2;
-                aM[3] = sm16[1][1] ^ NEG2;
             }
-            // Kbar_{n-1} and gamma_{n-1} (the other lane's previous chunk) are in their slot
-            if (n >= 1 && !__all_sync(0xffffffffu, wait_bar(bar(B_P2 + (n - 1) % NP), ((n - 1) / NP) & 1, flags))) break;
-            const uint32_t prev = slot(n + NP - 1), prev2 = slot(n + NP - 2);
-            uint32_t keep[8][4];  // with two finisher warps, half 0's W' fragments (stored once half 1 read K Gamma)
-            // this warp's 16-row halves of W: both with one finisher warp per lane, else its own
-            constexpr int NH = NFIN == 1 ? 2 : 1;
-            const int h0 = NFIN == 1 ? 0 : myhalf;
-            const bool defer = NFIN == 2 && myhalf == 0;  // store W' only once the other warp has read K Gamma
-            float hc[NH][2][4], hp[NH][2][4];  // this warp's columns of Kbar_{n-1} W^T and Kbar_{n-2} W'^T
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_HRDY + 2 * ln + xb), xpar, flags))) break;
+            // (H Phi^T)^T = [H^w (-T')^T | H^w (-s M)^T + s H^q]: B[k = m][n] = -T'[n][m] and
+            // -s M[n][m] come straight from the fragments of T' and s M
+            {
+                const uint4 ah = SM_AT(const uint4, hx + lane * 16);
+                const uint32_t aH[4] = {ah.x, ah.y, ah.z, ah.w};
+                const float4 q0 = SM_AT(const float4, hx + 512 + lane * 16), q1 = SM_AT(const float4, hx + 1024 + lane * 16);
+                float cf[4][4];
 #pragma unroll
-            for (int a = 0; a < NH; ++a)
+                for (int i = 0; i < 4; ++i) cf[i][0] = cf[i][1] = cf[i][2] = cf[i][3] = 0.f;
+                mma_f16(cf[0], aH, tw[0][0] ^ NEG2, tw[1][0] ^ NEG2);
+                mma_f16(cf[1], aH, tw[0][1] ^ NEG2, tw[1][1] ^ NEG2);
+                mma_f16(cf[2], aH, sm16[0][0] ^ NEG2, sm16[1][0] ^ NEG2);
+                mma_f16(cf[3], aH, sm16[0][1] ^ NEG2, sm16[1][1] ^ NEG2);
+                cf[2][0] = fmaf(sc, q0.x, cf[2][0]); cf[2][1] = fmaf(sc, q0.y, cf[2][1]);
+                cf[2][2] = fmaf(sc, q0.z, cf[2][2]); cf[2][3] = fmaf(sc, q0.w, cf[2][3]);
+                cf[3][0] = fmaf(sc, q1.x, cf[3][0]); cf[3][1] = fmaf(sc, q1.y, cf[3][1]);
+                cf[3][2] = fmaf(sc, q1.z, cf[3][2]); cf[3][3] = fmaf(sc, q1.w, cf[3][3]);
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) hc[a][i][j] = hp[a][i][j] = 0.f;
-#pragma unroll (W_UNROLL)
-            for (int kk = 0; kk < 8; ++kk) {
-                // this lane's matrix row for ldmatrix / stmatrix: W (or Z) row ri + 8 (mi & 1) [+ 16],
-                // channels 16 kk + 8 (mi >> 1) ..
-                const uint32_t za = sl + L_Z + sw128_32rows(ri + 8 * (mi & 1), 16 * kk + 8 * (mi >> 1));
-                uint32_t bz[4];
-                ldsm_x4_t(za, bz[0], bz[1], bz[2], bz[3]);  // B fragments of the K Gamma rows (k = row, n = channel)
-                // W' = W Diag(gamma_{n-1}) over channels 16 kk + 8 nt + 2 t + {0, 1}
-                float2 gv[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
-                if (n >= 1) {
-                    gv[0] = SM_AT(const float2, prev + L_GAM + (16 * kk + 2 * t) * 4);
-                    gv[1] = SM_AT(const float2, prev + L_GAM + (16 * kk + 8 + 2 * t) * 4);
-                }
-                uint32_t wq[NH][2][2], wpq[NH][2][2];  // f16 pairs of W and W' as B fragments: [half][row block][k half]
-#pragma unroll
-                for (int a = 0; a < NH; ++a) {
-                    const int half = h0 + a;
-                    float w[2][4];
-                    if (half == 0) {
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) w[nt][0] = w[nt][1] = w[nt][2] = w[nt][3] = 0.f;
-                    } else {
-                        uint32_t zq[4];
-                        ldsm_x4(za + 2048, zq[0], zq[1], zq[2], zq[3]);  // Q Gamma rows (16 on) in the accumulator layout
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            w[nt][0] = sc * h_lo(zq[2 * nt]);
-                            w[nt][1] = sc * h_hi(zq[2 * nt]);
-                            w[nt][2] = sc * h_lo(zq[2 * nt + 1]);
-                            w[nt][3] = sc * h_hi(zq[2 * nt + 1]);
-                        }
-                    }
-                    const uint32_t aPhi[4] = {half ? aM[0] : aT[0], half ? aM[1] : aT[1], half ? aM[2] : aT[2],
-                                              half ? aM[3] : aT[3]};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        mma_f16(w[nt], aPhi, bz[2 * nt], bz[2 * nt + 1]);
-                        wq[a][0][nt] = pack_f16(w[nt][0], w[nt][1]);
-                        wq[a][1][nt] = pack_f16(w[nt][2], w[nt][3]);
-                        wpq[a][0][nt] = pack_f16(w[nt][0] * gv[nt].x, w[nt][1] * gv[nt].y);
-                        wpq[a][1][nt] = pack_f16(w[nt][2] * gv[nt].x, w[nt][3] * gv[nt].y);
-                    }
-                }
-                if (defer) {
-                    keep[kk][0] = wpq[0][0][0];
-                    keep[kk][1] = wpq[0][1][0];
-                    keep[kk][2] = wpq[0][0][1];
-                    keep[kk][3] = wpq[0][1][1];
-                } else {
-                    __syncwarp();  // every lane's read of these rows is done before they are overwritten
-#pragma unroll
-                    for (int a = 0; a < NH; ++a)
-                        stsm_x4(za + 2048 * (h0 + a), wpq[a][0][0], wpq[a][1][0], wpq[a][0][1], wpq[a][1][1]);
-                }
-                if (n >= 1) {
-                    const uint32_t koff = raw_off(ri + 8 * (mi & 1), 16 * kk + 8 * (mi >> 1));  // A rows j, k = c
-                    uint32_t aK[4];
-                    ldsm_x4(prev + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
-#pragma unroll
-                    for (int a = 0; a < NH; ++a)
-#pragma unroll
-                        for (int rb = 0; rb < 2; ++rb) mma_f16(hc[a][rb], aK, wq[a][rb][0], wq[a][rb][1]);
-                    if (n >= 2) {
-                        ldsm_x4(prev2 + L_KB + koff, aK[0], aK[1], aK[2], aK[3]);
-#pragma unroll
-                        for (int a = 0; a < NH; ++a)
-#pragma unroll
-                            for (int rb = 0; rb < 2; ++rb) mma_f16(hp[a][rb], aK, wpq[a][rb][0], wpq[a][rb][1]);
-                    }
-                }
+                for (int nu = 0; nu < 4; nu += 2)
+                    stsm_x4_t(sl + L_CC + nu * 256 + stsm_row, pack_f16(cf[nu][0], cf[nu][1]), pack_f16(cf[nu][2], cf[nu][3]),
+                              pack_f16(cf[nu + 1][0], cf[nu + 1][1]), pack_f16(cf[nu + 1][2], cf[nu + 1][3]));
             }
-            bool ok = true;
-            if (NFIN == 2) {
-                if (myhalf == 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_ZREAD + 2 * ln + xb));  // the K Gamma rows are read
-                } else {
-                    ok = __all_sync(0xffffffffu, wait_bar(bar(B_ZREAD + 2 * ln + xb), xpar, flags));
-                    if (ok) {
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            stsm_x4(sl + L_Z + sw128_32rows(ri + 8 * (mi & 1), 16 * kk + 8 * (mi >> 1)), keep[kk][0],
-                                    keep[kk][1], keep[kk][2], keep[kk][3]);
-                    }
-                }
-            }
-            // (Kbar W^T)^T as [32 n][16 k] core matrices: column n of the 16 x 32 product is row n;
-            // each half's 16 columns
-#pragma unroll
-            for (int a = 0; a < NH; ++a) {
-                const int half = h0 + a;
-                stsm_x4_t(sl + L_CC + half * 512 + stsm_row, pack_f16(hc[a][0][0], hc[a][0][1]),
-                          pack_f16(hc[a][0][2], hc[a][0][3]), pack_f16(hc[a][1][0], hc[a][1][1]),
-                          pack_f16(hc[a][1][2], hc[a][1][3]));
-                stsm_x4_t(sl + L_HP + half * 512 + stsm_row, pack_f16(hp[a][0][0], hp[a][0][1]),
-                          pack_f16(hp[a][0][2], hp[a][0][3]), pack_f16(hp[a][1][0], hp[a][1][1]),
-                          pack_f16(hp[a][1][2], hp[a][1][3]));
-            }
-            if (!ok) break;
             tc::fence_async_smem();
             __syncwarp();
             if (lane == 0) {
+                mbar_arrive(bar(B_FDONE + 2 * ln + xb));
                 mbar_arrive(bar(B_PREP_FULL + n % NP));
-                if (n >= 1) mbar_arrive(bar(B_PREP_EMPTY + (n - 1) % NP));  // last read of Kbar_{n-1}, gamma_{n-1}
-                if (n >= 2) mbar_arrive(bar(B_PREP_EMPTY + (n - 2) % NP));  // last read of Kbar_{n-2}
             }
         }
     }

@@ -109,6 +109,14 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b
                  "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
                  : "memory");
 }
+__device__ __forceinline__ void mma_ts_tf32_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+                 "setp.ne.u32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+                 : "memory");
+}
 __device__ __forceinline__ void commit_w(uint32_t bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
