@@ -353,21 +353,25 @@ def copy_ceiling(h2d, d2h, dev):
     return res
 
 
-def run_launches(n):
-    """Run ``n`` forward passes of the benchmark workload (for profilers)."""
+def run_launches(n, workload=None, T=None):
+    """Run ``n`` forward passes of a workload (default: the benchmark's; ``T`` shortens it) for
+    profilers."""
     import torch
 
     import gated_linear_attention_kda_gb300 as kda
     import workloads as W
-    d = W.make(WORKLOAD)
+    name = workload or WORKLOAD
+    d = W.make(name, T=T)
     c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    nseq = d["q"].shape[0] if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    sdt = torch.float32 if d["initial_state"] is None else d["initial_state"].dtype
     out = torch.empty_like(c["v"])
-    fin = torch.empty(d["q"].shape[0], d["q"].shape[2], 128, 128, dtype=torch.float32, device="cuda")
+    fin = torch.empty(nseq, d["q"].shape[2], 128, 128, dtype=sdt, device="cuda")
     for _ in range(n):
         kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
                 d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
     kda.check_device_status()
-    print(f"ran {n} launches of {WORKLOAD}")
+    print(f"ran {n} launches of {name} (T={d['q'].shape[1]})")
 
 
 DECODE_B, DECODE_H = 128, 16   # 2048 fp32 states of 64 KiB: 134 MB, larger than L2
@@ -477,11 +481,13 @@ def main():
                     help="time single-token steps (kda_decode) instead and print their own JSON line")
     ap.add_argument("--workload", default=None,
                     help="kernel-only timing of another workload (workloads.ORDER) on its own JSON line")
+    ap.add_argument("--T", type=int, default=None,
+                    help="with --launches: tokens per batch row of the workload (a shorter case for profiling)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="kernel-only timing with raw q/k normalised in the kernel (KDA_FLAG_QK_L2NORM)")
     args = ap.parse_args()
     if args.launches:
-        run_launches(args.launches)
+        run_launches(args.launches, args.workload, args.T)
         return
     if args.decode:
         run_decode(args)
