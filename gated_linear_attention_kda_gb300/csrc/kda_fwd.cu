@@ -170,6 +170,54 @@ static cudaError_t launch_split(int vs, int64_t grid, cudaStream_t s, const CUte
 
 static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Per-device resources of kda_fwd_host, created on its first call on a device and kept until exit:
+// a memory pool whose staging allocations stay mapped between calls (release threshold at its
+// maximum), the streams and events of the pieces of a call, and pinned room for the rebased
+// sequence bounds of each piece. Calls of kda_fwd_host on one device are serialised by `mu`.
+constexpr int HOST_PIECES = 4;
+constexpr int HOST_CU_MAX = 1 << 16;  // sequences per piece
+struct HostLane {
+    std::mutex mu;
+    cudaMemPool_t pool = nullptr;
+    cudaStream_t streams[HOST_PIECES] = {};
+    cudaEvent_t start = nullptr, done[HOST_PIECES] = {};
+    int64_t *cu_host = nullptr;
+};
+
+static HostLane *host_lane(int dev, cudaError_t *err)
+{
+    static std::mutex mu;
+    static HostLane *lanes[256] = {};
+    if (dev < 0 || dev >= 256) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (lanes[dev]) {
+        *err = cudaSuccess;
+        return lanes[dev];
+    }
+    HostLane *hl = new HostLane;
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaError_t e = cudaMemPoolCreate(&hl->pool, &props);
+    if (e == cudaSuccess) {
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(hl->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    for (int i = 0; i < HOST_PIECES && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&hl->streams[i], cudaStreamNonBlocking);
+    for (int i = 0; i < HOST_PIECES && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&hl->done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hl->start, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaMallocHost(reinterpret_cast<void **>(&hl->cu_host), sizeof(int64_t) * HOST_PIECES * (HOST_CU_MAX + 1));
+    *err = e;
+    if (e != cudaSuccess) return nullptr;  // partially created resources are left to process exit
+    lanes[dev] = hl;
+    return hl;
+}
+
 // Snapshot of the device error word, taken and cleared in one atomic step by status_take_kernel.
 __device__ unsigned int g_dev_error_seen;
 
@@ -205,11 +253,14 @@ KDA_API kda_status kda_plan(int64_t units, int num_sms, int *v_split, int64_t *g
     return KDA_OK;
 }
 
-KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                              float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
-                              const void *initial_state, kda_dtype initial_dtype, void *final_state,
-                              kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
-                              int64_t H, int64_t K, int64_t V, uint32_t flags, void *stream)
+// kda_fwd_ex with an optional split of the V rows (`split_vs` 1, 2, 4 or 8; 0 = planned, or the
+// KDA_V_SPLIT override): kda_fwd_host runs the pieces of one call with the split of the whole call,
+// so its results equal kda_fwd's bit for bit.
+static kda_status fwd_impl(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                           void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                           const void *initial_state, kda_dtype initial_dtype, void *final_state, kda_dtype final_dtype,
+                           const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                           uint32_t flags, void *stream, int split_vs)
 {
     t_last_error.clear();
     if (flags & ~KDA_FLAG_QK_L2NORM) return fail(KDA_ERR_RANGE, "unknown option bits 0x%x", flags & ~KDA_FLAG_QK_L2NORM);
@@ -249,8 +300,8 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
     if ((A_log && !aligned(A_log, 4)) || (dt_bias && !aligned(dt_bias, 4)) || (cu_seqlens && !aligned(cu_seqlens, 8)))
         return fail(KDA_ERR_ALIGN, "A_log, dt_bias and cu_seqlens must be naturally aligned");
     // KDA_V_SPLIT (1, 2, 4 or 8) overrides the planned split of each state's V rows, for tuning and tests
-    int force_vs = 0;
-    if (const char *env = std::getenv("KDA_V_SPLIT")) {
+    int force_vs = split_vs;
+    if (const char *env = std::getenv("KDA_V_SPLIT"); env && !split_vs) {
         force_vs = std::atoi(env);
         if (force_vs != 1 && force_vs != 2 && force_vs != 4 && force_vs != 8)
             return fail(KDA_ERR_RANGE, "KDA_V_SPLIT must be 1, 2, 4 or 8 (got '%s')", env);
@@ -317,6 +368,16 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
                                       : launch_split<false>(vs, grid, s, mq, mk, mv, mg, p);
     if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(ce));
     return KDA_OK;
+}
+
+KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                              const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                              kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                              int64_t H, int64_t K, int64_t V, uint32_t flags, void *stream)
+{
+    return fwd_impl(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype, final_state,
+                    final_dtype, cu_seqlens, N, B, T, H, K, V, flags, stream, 0);
 }
 
 KDA_API kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
@@ -445,43 +506,112 @@ KDA_API kda_status kda_fwd_host(const void *q, const void *k, const void *v, con
                                 int64_t H, int64_t K, int64_t V, void *stream)
 {
     t_last_error.clear();
-    if (K != DH || V != DH || B < 1 || T < 0 || H < 1 || (cu_seqlens && N < 1))
+    if (K != DH || V != DH || B < 1 || T < 0 || H < 1 || (cu_seqlens && (N < 1 || B != 1)))
         return fail(KDA_ERR_SHAPE, "bad sizes");
+    if (cu_seqlens)  // the host copy of the sequence bounds is read here to cut the call into pieces
+        for (int64_t i = 0; i < N; ++i)
+            if (cu_seqlens[i] < 0 || cu_seqlens[i + 1] < cu_seqlens[i] || cu_seqlens[i + 1] > T || cu_seqlens[0] != 0 ||
+                cu_seqlens[N] != T)
+                return fail(KDA_ERR_SHAPE, "cu_seqlens must rise from 0 to T");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    HostLane *hl = e == cudaSuccess ? host_lane(dev, &e) : nullptr;
+    if (!hl) return fail(KDA_ERR_LAUNCH, "staging set-up failed: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> call_lock(hl->mu);
     const int64_t total = B * T, nseq = cu_seqlens ? N : B;
     const size_t act = static_cast<size_t>(total) * H * DH * 2, bet = static_cast<size_t>(total) * H * 2;
-    const size_t st_in = initial_state ? static_cast<size_t>(nseq) * H * DH * DH * (initial_dtype == KDA_DTYPE_FP32 ? 4 : 2) : 0;
-    const size_t st_out = final_state ? static_cast<size_t>(nseq) * H * DH * DH * (final_dtype == KDA_DTYPE_FP32 ? 4 : 2) : 0;
-    const size_t cub = cu_seqlens ? static_cast<size_t>(N + 1) * 8 : 0;
+    const size_t sti = initial_state ? (initial_dtype == KDA_DTYPE_FP32 ? 4 : 2) : 0;
+    const size_t sto = final_state ? (final_dtype == KDA_DTYPE_FP32 ? 4 : 2) : 0;
+    const size_t st_row = static_cast<size_t>(H) * DH * DH;  // state elements per sequence
+    const size_t cub = cu_seqlens ? static_cast<size_t>(N + 1 + HOST_PIECES) * 8 : 0;  // each piece's rebased bounds
     const size_t al = A_log ? static_cast<size_t>(H) * 4 : 0, db = dt_bias ? static_cast<size_t>(H) * DH * 4 : 0;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t sizes[] = {act, act, act, act, bet, act, al, db, st_in, st_out, cub};
+    const size_t sizes[] = {act, act, act, act, bet, act, al, db, nseq * st_row * sti, nseq * st_row * sto, cub};
     size_t off[11], tot = 0;
     for (int i = 0; i < 11; ++i) {
         off[i] = tot;
         tot += up(sizes[i]);
     }
-    uint8_t *d = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&d), tot ? tot : 256, s);
-    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "device staging allocation failed: %s", cudaGetErrorString(e));
-    const void *src[] = {q, k, v, g, beta, nullptr, A_log, dt_bias, initial_state, nullptr, cu_seqlens};
-    for (int i = 0; i < 11 && e == cudaSuccess; ++i)
-        if (src[i] && sizes[i]) e = cudaMemcpyAsync(d + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, s);
-    kda_status st = KDA_ERR_LAUNCH;
-    if (e == cudaSuccess) {
-        st = kda_fwd(d + off[0], d + off[1], d + off[2], d + off[3], d + off[4], scale, d + off[5],
-                     A_log ? reinterpret_cast<const float *>(d + off[6]) : nullptr,
-                     dt_bias ? reinterpret_cast<const float *>(d + off[7]) : nullptr, lower_bound,
-                     initial_state ? d + off[8] : nullptr, initial_dtype, final_state ? d + off[9] : nullptr,
-                     final_dtype, cu_seqlens ? reinterpret_cast<const int64_t *>(d + off[10]) : nullptr, N, B, T, H, K,
-                     V, stream);
-        if (st == KDA_OK) {
-            if (act) e = cudaMemcpyAsync(out, d + off[5], act, cudaMemcpyDeviceToHost, s);
-            if (e == cudaSuccess && st_out) e = cudaMemcpyAsync(final_state, d + off[9], st_out, cudaMemcpyDeviceToHost, s);
-            if (e != cudaSuccess) st = fail(KDA_ERR_LAUNCH, "device-to-host copy failed: %s", cudaGetErrorString(e));
+    // the whole call's V-row split, used by every piece (identical kernels, identical results)
+    int vs = 1;
+    int64_t grid = 0;
+    plan(nseq * H, nsm, &vs, &grid);
+    if (const char *env = std::getenv("KDA_V_SPLIT")) {  // a bad value is reported by the forward call itself
+        const int ev = std::atoi(env);
+        vs = (ev == 1 || ev == 2 || ev == 4 || ev == 8) ? ev : 0;
+    }
+    // pieces: groups of batch rows (or of sequences, by token count), each on its own stream, so the
+    // copies of one piece overlap the kernel and copies of the others
+    int np = static_cast<int>(nseq < HOST_PIECES ? nseq : HOST_PIECES);
+    if (total == 0) np = 1;
+    int64_t first[HOST_PIECES + 1];  // first batch row / sequence of each piece
+    first[0] = 0;
+    for (int i = 1; i < np; ++i) {
+        if (!cu_seqlens) {
+            first[i] = nseq * i / np;
+        } else {  // the first sequence that starts at or after i / np of the tokens
+            int64_t j = first[i - 1] + 1;
+            while (j < nseq - (np - i) && cu_seqlens[j] * np < total * i) ++j;
+            first[i] = j;
         }
-    } else {
-        fail(KDA_ERR_LAUNCH, "host-to-device copy failed: %s", cudaGetErrorString(e));
+    }
+    first[np] = nseq;
+    uint8_t *d = nullptr;
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&d), tot ? tot : 256, hl->pool, s);
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "device staging allocation failed: %s", cudaGetErrorString(e));
+    if (al) e = cudaMemcpyAsync(d + off[6], A_log, al, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && db) e = cudaMemcpyAsync(d + off[7], dt_bias, db, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(hl->start, s);
+    kda_status st = KDA_OK;
+    for (int pi = 0; pi < np && e == cudaSuccess && st == KDA_OK; ++pi) {
+        cudaStream_t ps = hl->streams[pi];
+        const int64_t s0 = first[pi], s1 = first[pi + 1];
+        const int64_t t0 = cu_seqlens ? cu_seqlens[s0] : s0 * T, t1 = cu_seqlens ? cu_seqlens[s1] : s1 * T;
+        const size_t ao = static_cast<size_t>(t0) * H * DH * 2, an = static_cast<size_t>(t1 - t0) * H * DH * 2;
+        const size_t bo = static_cast<size_t>(t0) * H * 2, bn = static_cast<size_t>(t1 - t0) * H * 2;
+        e = cudaStreamWaitEvent(ps, hl->start, 0);
+        const void *src[4] = {q, k, v, g};
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            if (an) e = cudaMemcpyAsync(d + off[i] + ao, static_cast<const uint8_t *>(src[i]) + ao, an, cudaMemcpyHostToDevice, ps);
+        if (e == cudaSuccess && bn)
+            e = cudaMemcpyAsync(d + off[4] + bo, static_cast<const uint8_t *>(beta) + bo, bn, cudaMemcpyHostToDevice, ps);
+        if (e == cudaSuccess && sti)
+            e = cudaMemcpyAsync(d + off[8] + s0 * st_row * sti, static_cast<const uint8_t *>(initial_state) + s0 * st_row * sti,
+                                (s1 - s0) * st_row * sti, cudaMemcpyHostToDevice, ps);
+        const int64_t *dcu = nullptr;
+        if (e == cudaSuccess && cu_seqlens) {  // this piece's bounds, rebased to its first token
+            int64_t *host_cu = hl->cu_host + pi * (HOST_CU_MAX + 1);
+            if (s1 - s0 > HOST_CU_MAX) {
+                st = fail(KDA_ERR_SHAPE, "kda_fwd_host: at most %d sequences per piece", HOST_CU_MAX);
+                break;
+            }
+            for (int64_t i = s0; i <= s1; ++i) host_cu[i - s0] = cu_seqlens[i] - t0;
+            dcu = reinterpret_cast<const int64_t *>(d + off[10]) + s0 + pi;  // entries [s0 + pi, s1 + pi]
+            e = cudaMemcpyAsync(const_cast<int64_t *>(dcu), host_cu, (s1 - s0 + 1) * 8, cudaMemcpyHostToDevice, ps);
+        }
+        if (e != cudaSuccess) break;
+        const int64_t pB = cu_seqlens ? 1 : s1 - s0, pT = cu_seqlens ? t1 - t0 : T;
+        st = fwd_impl(d + off[0] + ao, d + off[1] + ao, d + off[2] + ao, d + off[3] + ao, d + off[4] + bo, scale,
+                      d + off[5] + ao, A_log ? reinterpret_cast<const float *>(d + off[6]) : nullptr,
+                      dt_bias ? reinterpret_cast<const float *>(d + off[7]) : nullptr, lower_bound,
+                      initial_state ? d + off[8] + s0 * st_row * sti : nullptr, initial_dtype,
+                      final_state ? d + off[9] + s0 * st_row * sto : nullptr, final_dtype, dcu, s1 - s0, pB, pT, H, K, V, 0u,
+                      ps, vs);
+        if (st != KDA_OK) break;
+        if (an) e = cudaMemcpyAsync(static_cast<uint8_t *>(out) + ao, d + off[5] + ao, an, cudaMemcpyDeviceToHost, ps);
+        if (e == cudaSuccess && sto)
+            e = cudaMemcpyAsync(static_cast<uint8_t *>(final_state) + s0 * st_row * sto, d + off[9] + s0 * st_row * sto,
+                                (s1 - s0) * st_row * sto, cudaMemcpyDeviceToHost, ps);
+        if (e == cudaSuccess) e = cudaEventRecord(hl->done[pi], ps);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hl->done[pi], 0);
+    }
+    if (e != cudaSuccess && st == KDA_OK) st = fail(KDA_ERR_LAUNCH, "staging copy failed: %s", cudaGetErrorString(e));
+    // the caller's stream waits for every piece (also after a failure, before the memory is freed)
+    for (int pi = 0; pi < np; ++pi) {
+        cudaEventRecord(hl->done[pi], hl->streams[pi]);
+        cudaStreamWaitEvent(s, hl->done[pi], 0);
     }
     cudaFreeAsync(d, s);
     cudaError_t se = cudaStreamSynchronize(s);

@@ -189,11 +189,23 @@ KDA_API kda_status kda_fwd_packed(const kda_fwd_args *a, void *stream);
 /*
  * kda_fwd_host -- the same operation on HOST buffers (same layouts and
  * arguments as kda_fwd, every pointer a host pointer; pinned memory gives
- * the fastest copies). It stages the inputs in stream-ordered device memory
- * that it allocates for the call, runs kda_fwd on `stream`, copies `out` and
- * `final_state` back, frees the staging memory and synchronises `stream`
- * before it returns. This is the end-to-end entry point for callers whose
+ * the fastest copies). It stages the inputs in device memory, runs the
+ * forward pass, copies `out` and `final_state` back and synchronises
+ * `stream` before it returns: the end-to-end entry point for callers whose
  * tensors live in host memory.
+ *   The call is cut into up to four pieces -- groups of batch rows, or in
+ * varlen mode groups of whole sequences of about equal token count -- each on
+ * a stream of its own, so that the host-to-device copy of one piece overlaps
+ * the kernel and the device-to-host copy of the others. Every piece uses the
+ * V-row split planned for the whole call, so the results equal kda_fwd's bit
+ * for bit. In varlen mode cu_seqlens is a host array here; it must rise from
+ * 0 to T (else KDA_ERR_SHAPE before anything is copied).
+ *   On its first call on a device it creates, and keeps until the process
+ * exits, a stream-ordered memory pool for the staging buffers (they stay
+ * mapped between calls), four streams and five events, and a small pinned
+ * host buffer; calls on one device are serialised. Work already queued on
+ * `stream` is ordered before the call, and the call's work before later work
+ * on `stream`.
  */
 KDA_API kda_status kda_fwd_host(const void *q, const void *k, const void *v, const void *g,
                                 const void *beta, float scale, void *out,

@@ -208,3 +208,17 @@ def test_python_wrapper_rejects_tensors_on_another_device(kda):
     kda._same_device(q.device, (("k", q), ("state", st)))  # same device: accepted
     with pytest.raises(ValueError, match="state is on meta"):
         kda._same_device(q.device, (("k", q), ("state", st.to("meta"))))
+
+
+def test_host_entry_checks_its_host_cu_seqlens_before_any_copy(kda):
+    """kda_fwd_host reads cu_seqlens on the host (to cut the call into pieces): bounds that do not
+    rise from 0 to T are KDA_ERR_SHAPE before any CUDA call."""
+    import ctypes
+    import numpy as np
+    lib = kda.library()
+    for bad in ([0, 5, 3, 8], [1, 4, 8], [0, 4, 9], [0, 4, 7]):
+        cu = np.array(bad, dtype=np.int64)
+        st = lib.kda_fwd_host(None, None, None, None, None, 1.0, None, None, None, -5.0, None, 0, None, 0,
+                              cu.ctypes.data_as(ctypes.c_void_p), len(bad) - 1, 1, 8, 2, 128, 128, None)
+        assert st == 2, bad  # KDA_ERR_SHAPE
+        assert b"cu_seqlens" in lib.kda_last_error()

@@ -225,18 +225,29 @@ def test_empty_varlen_call_and_its_cu_seqlens_check():
     torch.cuda.synchronize()
 
 
-def test_host_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("case", ["b2", "b8_four_pieces", "varlen_pieces", "empty"])
+def test_host_entry_point_matches_device_entry_point(case):
+    """kda_fwd_host (pinned host buffers, the call cut into pieces on their own streams) gives
+    kda_fwd's results bit for bit: the pieces run the V-row split of the whole call."""
     import gated_linear_attention_kda_gb300 as kda
-    d = W.make("b2_t128_h8", T=45)
-    o_dev, s_dev = run_gpu(d)
-    out = torch.empty_like(d["v"]).pin_memory()
-    fin = torch.empty_like(d["initial_state"]).pin_memory()
+    fdt = "fp32"
+    if case == "b2":
+        d = W.make("b2_t128_h8", T=45)
+    elif case == "b8_four_pieces":
+        d = W.make("b2_t128_h8", B=8, T=70, H=12)
+    elif case == "varlen_pieces":
+        d = W.make("varlen_n16_h32", lengths=[5, 37, 16, 1, 0, 23, 64, 40, 200, 17], H=12)
+        fdt = "bf16"
+    else:
+        d = W.make("b2_t128_h8", B=3, T=0)
+    o_dev, s_dev = run_gpu(d, final_dtype=fdt)
+    out = torch.full_like(d["v"], float("nan")).pin_memory()
+    fin = torch.full_like(d["initial_state"], float("nan")).pin_memory()
     pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     kda.fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], d["scale"], out, pin["A_log"],
-                 pin["dt_bias"], d["lower_bound"], pin["initial_state"], fin)
+                 pin["dt_bias"], d["lower_bound"], pin["initial_state"], fin, pin["cu_seqlens"])
     assert np.array_equal(out.float().double().numpy(), o_dev)
-    assert np.array_equal(fin.double().numpy(), s_dev)
-
+    assert np.array_equal(fin.float().double().numpy(), s_dev)
 
 
 @pytest.mark.parametrize("entry", ["fwd_flat", "fwd_packed"])
