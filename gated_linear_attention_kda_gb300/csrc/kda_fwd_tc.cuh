@@ -573,6 +573,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
+            // with in-kernel q/k normalisation the row scales come from the raw tile alone: they are
+            // formed here, while the lane would otherwise wait for its slot
+            float sk[4], sq[4];
+            if constexpr (QKN) {
+                uint2 kn[4], qn[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = r0 + i;
+                    const uint2 kraw = SM_AT(const uint2, raw + OFF_K + raw_off(r, c0));
+                    kn[i] = r < Lv ? kraw : make_uint2(0u, 0u);
+                    qn[i] = SM_AT(const uint2, raw + OFF_Q + raw_off(r, c0));
+                }
+                qk_row_scales(kn, qn, lane, sk, sq);
+            }
             if (!wait_bar(bar(B_PREP_EMPTY + n % NP), ((n / NP) & 1) ^ 1, flags)) failed = true;
             // the finisher is done with this buffer's previous chunk
             if (!wait_bar(bar(B_FDONE + 2 * ln + xb), xpar ^ 1, flags)) failed = true;
@@ -629,8 +643,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qwv[i] = SM_AT(const uint2, raw + OFF_Q + raw_off(r, c0));
                 vwv[i] = SM_AT(const uint2, raw + OFF_V + raw_off(r, c0));
             }
-            float sk[4], sq[4];
-            if constexpr (QKN) qk_row_scales(kwv, qwv, lane, sk, sq);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = r0 + i;
