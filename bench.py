@@ -423,16 +423,19 @@ def run_decode(args):
 
 
 def run_variant(args):
-    """Kernel-only timing of one workload (``--workload``), optionally with raw q/k normalised in
-    the kernel (``--qk-norm``): its own JSON line, tokens/s and the HBM fraction of the
-    algorithmic bytes. Not the benchmark line."""
+    """Kernel-only timing of one workload (``--workload``, reshaped by ``--B/--T/--H``), optionally
+    with raw q/k normalised in the kernel (``--qk-norm``), 32-token chunks (``--chunk 32``) or a
+    forced split of the V rows (``--v-split``): its own JSON line, tokens/s and the HBM fraction of
+    the algorithmic bytes. Not the benchmark line."""
     import torch
 
     import gated_linear_attention_kda_gb300 as kda
     import workloads as W
     torch.cuda.set_device(0)
     name = args.workload or WORKLOAD
-    d = W.make(name, raw_qk=args.qk_norm)
+    if args.v_split:
+        os.environ["KDA_V_SPLIT"] = str(args.v_split)
+    d = W.make(name, raw_qk=args.qk_norm, B=args.B, T=args.T, H=args.H)
     c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     B, T, H = d["q"].shape[0], d["q"].shape[1], d["q"].shape[2]
     nseq = B if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
@@ -442,7 +445,7 @@ def run_variant(args):
 
     def step():
         kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
-                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], qk_l2norm=args.qk_norm)
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], qk_l2norm=args.qk_norm, chunk=args.chunk)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -465,7 +468,8 @@ def run_variant(args):
         "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic", "config": {"workload": name, "B": B, "T": T, "H": H, "sequences": nseq,
-                                        "qk_l2norm": bool(args.qk_norm)},
+                                        "qk_l2norm": bool(args.qk_norm), "chunk": args.chunk,
+                                        "v_split": args.v_split or kda.plan(nseq * H, torch.cuda.get_device_properties(0).multi_processor_count)[0]},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": src, "algorithmic_bytes_per_launch": nbytes},
         "gpu_launches": args.steps}), flush=True)
@@ -484,7 +488,14 @@ def main():
     ap.add_argument("--workload", default=None,
                     help="kernel-only timing of another workload (workloads.ORDER) on its own JSON line")
     ap.add_argument("--T", type=int, default=None,
-                    help="with --launches: tokens per batch row of the workload (a shorter case for profiling)")
+                    help="tokens per batch row instead of the workload's (with --launches: a shorter case for "
+                         "profiling; otherwise kernel-only timing of the reshaped workload)")
+    ap.add_argument("--B", type=int, default=None, help="batch rows instead of the workload's (kernel-only timing)")
+    ap.add_argument("--H", type=int, default=None, help="heads instead of the workload's (kernel-only timing)")
+    ap.add_argument("--chunk", type=int, choices=[16, 32], default=16,
+                    help="kernel-only timing with 32-token chunks (KDA_FLAG_CHUNK32, the chunk-size ablation)")
+    ap.add_argument("--v-split", type=int, choices=[1, 2, 4, 8], default=None,
+                    help="kernel-only timing with the V rows of each state split over this many CTAs (KDA_V_SPLIT)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="kernel-only timing with raw q/k normalised in the kernel (KDA_FLAG_QK_L2NORM)")
     args = ap.parse_args()
@@ -494,7 +505,7 @@ def main():
     if args.decode:
         run_decode(args)
         return
-    if args.workload or args.qk_norm:
+    if args.workload or args.qk_norm or args.chunk != 16 or args.v_split or args.B or args.H or args.T:
         run_variant(args)
         return
     if args.impl == "reference":

@@ -34,6 +34,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
           5: "KDA_ERR_STATE_MISMATCH", 6: "KDA_ERR_ALIGN", 7: "KDA_ERR_LAUNCH", 8: "KDA_ERR_DEVICE"}
 DTYPE_NONE, DTYPE_BF16, DTYPE_FP32 = 0, 1, 2
 FLAG_QK_L2NORM = 1  # KDA_FLAG_QK_L2NORM: q and k L2-normalised per (token, head) inside the kernel
+FLAG_CHUNK32 = 2    # KDA_FLAG_CHUNK32: 32-token chunks (the chunk-size ablation)
 _P, _F, _I64, _I = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int
 FWD_ARGTYPES = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]
 _lib.kda_fwd.argtypes = FWD_ARGTYPES
@@ -148,6 +149,12 @@ def _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
     return B, T, H, K, V, N
 
 
+def _flags(qk_l2norm, chunk):
+    if chunk not in (16, 32):
+        raise ValueError(f"chunk must be 16 or 32, got {chunk}")
+    return (FLAG_QK_L2NORM if qk_l2norm else 0) | (FLAG_CHUNK32 if chunk == 32 else 0)
+
+
 def _same_device(dev, named):
     """Every given tensor must live on ``dev`` (q's device): the library launches on that device
     and dereferences every pointer there, so a tensor on another GPU is rejected here."""
@@ -157,11 +164,14 @@ def _same_device(dev, named):
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
-        initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False):
+        initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False, chunk=16):
     """Chunked KDA forward on the current CUDA stream. Writes ``out`` (and
     ``final_state`` if given) in place and returns ``(out, final_state)``.
     ``qk_l2norm=True`` L2-normalises q and k per (token, head) inside the
-    kernel (``kda_fwd_ex`` with ``KDA_FLAG_QK_L2NORM``); otherwise ``kda_fwd``."""
+    kernel (``KDA_FLAG_QK_L2NORM``); ``chunk=32`` runs 32-token chunks
+    (``KDA_FLAG_CHUNK32``). Either goes through ``kda_fwd_ex``, the plain
+    call through ``kda_fwd``."""
+    flags = _flags(qk_l2norm, chunk)
     B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
                                  cu_seqlens, cuda=True)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
@@ -171,8 +181,8 @@ def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0
             _ptr(cu_seqlens), N, B, T, H, K, V)
     with torch.cuda.device(q.device):
         stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
-        if qk_l2norm:
-            st = _lib.kda_fwd_ex(*args, FLAG_QK_L2NORM, stream)
+        if flags:
+            st = _lib.kda_fwd_ex(*args, flags, stream)
         else:
             st = _lib.kda_fwd(*args, stream)
     _raise(st)
@@ -196,8 +206,9 @@ def fwd_flat(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound
 
 
 def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
-               initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False):
+               initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False, chunk=16):
     """``fwd`` through the argument-struct entry point ``kda_fwd_packed``."""
+    flags = _flags(qk_l2norm, chunk)
     B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
                                  cu_seqlens, cuda=True)
     a = FwdArgs()
@@ -208,7 +219,7 @@ def fwd_packed(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bou
     a.initial_dtype, a.final_dtype = _state_code(initial_state), _state_code(final_state)
     a.scale, a.lower_bound = float(scale), float(lower_bound)
     a.N, a.B, a.T, a.H, a.K, a.V = N, B, T, H, K, V
-    a.flags = FLAG_QK_L2NORM if qk_l2norm else 0
+    a.flags = flags
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = _lib.kda_fwd_packed(ctypes.byref(a), ctypes.c_void_p(stream))

@@ -59,6 +59,7 @@
 #include "kda.h"
 #include "kda_common.cuh"
 #include "kda_fwd_mma.cuh"
+#include "kda_fwd_mma32.cuh"
 #include "kda_fwd_tc.cuh"
 #include "kda_probe.cuh"
 #include "kda_decode.cuh"
@@ -154,6 +155,35 @@ static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q,
     }
     tcs::kda_fwd_tc_kernel<QKN><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
+}
+
+template <int NS>
+static cudaError_t launch32(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
+                            const CUtensorMap &v, const CUtensorMap &g, const Params &p)
+{
+    static thread_local int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(v32::kda_fwd32_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, v32::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    v32::kda_fwd32_kernel<NS><<<static_cast<unsigned>(grid), 32 * (1 + 4 * v32::NP + NS), v32::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    return cudaGetLastError();
+}
+
+// 32-token chunks (KDA_FLAG_CHUNK32): the warp-MMA kernel at every split, 128 / split V rows per CTA
+static cudaError_t launch_split32(int vs, int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
+                                  const CUtensorMap &v, const CUtensorMap &g, const Params &p)
+{
+    switch (vs) {
+        case 1: return launch32<8>(grid, s, q, k, v, g, p);
+        case 2: return launch32<4>(grid, s, q, k, v, g, p);
+        case 4: return launch32<2>(grid, s, q, k, v, g, p);
+        default: return launch32<1>(grid, s, q, k, v, g, p);
+    }
 }
 
 template <bool QKN>
@@ -263,7 +293,10 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
                            uint32_t flags, void *stream, int split_vs)
 {
     t_last_error.clear();
-    if (flags & ~KDA_FLAG_QK_L2NORM) return fail(KDA_ERR_RANGE, "unknown option bits 0x%x", flags & ~KDA_FLAG_QK_L2NORM);
+    constexpr uint32_t known = KDA_FLAG_QK_L2NORM | KDA_FLAG_CHUNK32;
+    if (flags & ~known) return fail(KDA_ERR_RANGE, "unknown option bits 0x%x", flags & ~known);
+    if ((flags & KDA_FLAG_CHUNK32) && (flags & KDA_FLAG_QK_L2NORM))
+        return fail(KDA_ERR_RANGE, "KDA_FLAG_CHUNK32 does not combine with KDA_FLAG_QK_L2NORM");
     if (K != DH || V != DH) return fail(KDA_ERR_SHAPE, "K and V must be 128 (got K=%lld V=%lld)", (long long)K, (long long)V);
     if (B < 1 || T < 0 || H < 1) return fail(KDA_ERR_SHAPE, "bad sizes B=%lld T=%lld H=%lld", (long long)B, (long long)T, (long long)H);
     if (cu_seqlens && (B != 1 || N < 1))
@@ -364,8 +397,11 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
         grid = nseq * H * vs;
     }
     p.vsplit = vs;
-    ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, p)
-                                      : launch_split<false>(vs, grid, s, mq, mk, mv, mg, p);
+    if (flags & KDA_FLAG_CHUNK32)
+        ce = launch_split32(vs, grid, s, mq, mk, mv, mg, p);
+    else
+        ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, p)
+                                          : launch_split<false>(vs, grid, s, mq, mk, mv, mg, p);
     if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "kernel launch failed: %s", cudaGetErrorString(ce));
     return KDA_OK;
 }

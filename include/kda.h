@@ -83,9 +83,21 @@ typedef enum kda_dtype {
  *                       in fp32 from the bf16 inputs (the inputs are not
  *                       modified). The pages do not say whether q and k arrive
  *                       normalised; without this bit they are used as given.
+ *   KDA_FLAG_CHUNK32    run the forward pass with 32-token chunks (the
+ *                       warp-MMA kernel at the planned split of the V rows,
+ *                       the exponent reference after the chunk's 16th token,
+ *                       the 32x32 inverse from two 16x16 blocks) instead of
+ *                       CHUNK = 16: the chunk-size ablation of [CHUNK] "Why
+ *                       CHUNK Size Determines Numerical Stability". Results
+ *                       agree with the CHUNK = 16 path within the stated
+ *                       tolerance, not bit for bit. Forward entry points
+ *                       with option bits only (kda_fwd_ex, kda_fwd_packed);
+ *                       with KDA_FLAG_QK_L2NORM, or in kda_decode_ex, it is
+ *                       KDA_ERR_RANGE.
  * Any other bit is KDA_ERR_RANGE.
  */
 #define KDA_FLAG_QK_L2NORM 1u
+#define KDA_FLAG_CHUNK32 2u
 
 /*
  * kda_fwd -- the chunked KDA forward pass (CHUNK = 16 [CHUNK]).

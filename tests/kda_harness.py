@@ -16,7 +16,7 @@ def to_dev(d, dev="cuda"):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None, qk_l2norm=False):
+def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None, qk_l2norm=False, chunk=16):
     import gated_linear_attention_kda_gb300 as kda
     c = to_dev(d)
     out = torch.full_like(c["v"], float("nan"))
@@ -30,7 +30,7 @@ def run_gpu(d, final_dtype="fp32", in_place=False, lower_bound=None, scale=None,
         fin = torch.full((nseq, H, 128, 128), float("nan"), dtype=_DT[final_dtype], device="cuda")
     kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"] if scale is None else scale, out,
             c["A_log"], c["dt_bias"], d["lower_bound"] if lower_bound is None else lower_bound, init, fin,
-            c["cu_seqlens"], qk_l2norm=qk_l2norm)
+            c["cu_seqlens"], qk_l2norm=qk_l2norm, chunk=chunk)
     kda.check_device_status()
     o = out.float().cpu().double().numpy()
     s = None if fin is None else fin.float().cpu().double().numpy()

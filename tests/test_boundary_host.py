@@ -125,12 +125,13 @@ def test_plain_c_program_uses_the_abi(kda, tmp_path):
     assert r.stdout.count("ok ") == 11
 
 
-@pytest.mark.parametrize("flags", [2, 4, 0x80000000, 3])
+@pytest.mark.parametrize("flags", [2, 4, 0x80000000, 3, 6])
 def test_unknown_option_bits_are_rejected_on_the_host(kda, flags):
     lib = kda.library()
-    st = lib.kda_fwd_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0,
-                        None, 0, 1, 16, 1, 128, 128, flags, None)
-    assert st == 4 and b"option bits" in lib.kda_last_error()
+    if flags & ~3:  # KDA_FLAG_QK_L2NORM and KDA_FLAG_CHUNK32 are the forward pass's bits
+        st = lib.kda_fwd_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0,
+                            None, 0, 1, 16, 1, 128, 128, flags, None)
+        assert st == 4 and b"option bits" in lib.kda_last_error()
     st = lib.kda_decode_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, 0x10000, 2,
                            2, 3, 128, 128, flags, None)
     assert st == 4 and b"option bits" in lib.kda_last_error()
@@ -142,6 +143,16 @@ def test_option_entry_points_validate_like_the_plain_ones(kda):
                           None, 0, 1, 16, 1, 64, 128, 1, None) == 2  # K != 128 with the flag set
     assert lib.kda_decode_ex(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 2,
                              2, 3, 128, 128, 1, None) == 1  # state NULL
+
+
+def test_chunk32_flag_is_validated_on_the_host(kda):
+    lib = kda.library()
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0, None, 0, 1, 16, 1)
+    assert lib.kda_fwd_ex(*args, 128, 128, 3, None) == 4  # with KDA_FLAG_QK_L2NORM: KDA_ERR_RANGE
+    assert b"does not combine" in lib.kda_last_error()
+    assert lib.kda_fwd_ex(*args, 64, 128, 2, None) == 2  # K != 128: KDA_ERR_SHAPE, as without the flag
+    with pytest.raises(ValueError, match="chunk must be 16 or 32"):
+        kda.fwd(*([None] * 7), chunk=64)
 
 
 @pytest.mark.parametrize("value", ["3", "0", "16", "x"])
