@@ -66,6 +66,8 @@ _lib.kda_decode_ex.argtypes = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, _P, _I, _
 _lib.kda_decode_ex.restype = _I
 _lib.kda_probe_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P]
 _lib.kda_probe_chunk.restype = _I
+_lib.kda_probe_wait_timeout.argtypes = [_I, _P, _P]
+_lib.kda_probe_wait_timeout.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
 _lib.kda_check_device_status.argtypes = [_P]
 _lib.kda_check_device_status.restype = _I
@@ -276,6 +278,19 @@ def probe_chunk(q, k, g, beta, A_log=None, dt_bias=None, lower_bound=-5.0, rows=
                                   _ptr(o["P"]), _ptr(o["T"]), ctypes.c_void_p(stream))
     _raise(st)
     return o
+
+def probe_wait_timeout(polls, device=None):
+    """Test hook: run the kernels' bounded pipeline wait out on purpose (``kda_probe_wait_timeout``)
+    with ``polls`` polls. Returns the three result words: (wait 0 succeeded, wait 1 succeeded,
+    abort flag). The device error word then carries the timeout bit for ``check_device_status``."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    res = torch.full((3,), -1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = _lib.kda_probe_wait_timeout(int(polls), _ptr(res), ctypes.c_void_p(stream))
+    _raise(st)
+    return [int(x) for x in res.cpu()]
+
 
 def fwd_host(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
              initial_state=None, final_state=None, cu_seqlens=None, device=None):

@@ -50,11 +50,13 @@ constexpr uint32_t WAIT_HINT_NS = 20000;
 constexpr int WAIT_LIMIT = 1 << 18;
 
 // Slow path of wait_bar, kept out of line: the kernels wait at many sites and
-// inlined copies of the loop would crowd the instruction cache.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+// inlined copies of the loop would crowd the instruction cache. `limit` polls
+// (WAIT_LIMIT in the kernels; the wait-timeout probe passes a shorter one).
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           int limit = WAIT_LIMIT)
 {
 #pragma unroll 1
-    for (int i = 0; i < WAIT_LIMIT; ++i) {
+    for (int i = 0; i < limit; ++i) {
         if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return true;
         if (*abort_flag) return false;
     }

@@ -516,6 +516,19 @@ KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, 
     return KDA_OK;
 }
 
+KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream)
+{
+    t_last_error.clear();
+    if (!result) return fail(KDA_ERR_NULL, "kda_probe_wait_timeout: result is required");
+    if (polls < 1 || polls > WAIT_LIMIT)
+        return fail(KDA_ERR_RANGE, "kda_probe_wait_timeout: polls must lie in 1..%d (got %d)", WAIT_LIMIT, polls);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    probe::kda_probe_wait_kernel<<<1, 64, 0, s>>>(polls, result);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "probe launch failed: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}
+
 KDA_API kda_status kda_check_device_status(void *stream)
 {
     t_last_error.clear();

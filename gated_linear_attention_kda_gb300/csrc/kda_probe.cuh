@@ -96,5 +96,31 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// The bounded pipeline wait run out on purpose, with nothing left in flight: two lanes each wait
+// on an mbarrier that nothing ever arrives on, through the kernels' own slow wait path with
+// `polls` polls. Expected: both waits give up (result[0..1] = 0), the first to run out flags
+// DEVERR_TIMEOUT in the device error word and sets the CTA's abort flag (result[2] = 1), which
+// ends the other wait early; the kernel then returns normally and the context stays usable.
+__global__ void __launch_bounds__(64) kda_probe_wait_kernel(int polls, int *result)
+{
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (lane == 0) {
+        const uint32_t bar = smem_u32(&bars[warp]);
+        const bool ok = mbar_try_wait(bar, 0) || wait_bar_slow(bar, 0, &abort_flag, polls);
+        result[warp] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) result[2] = abort_flag;
+}
+
 }  // namespace probe
 }  // namespace kda

@@ -283,6 +283,24 @@ KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, 
                                    const float *A_log, const float *dt_bias, float lower_bound, int rows,
                                    float *G2, float *beta_act, float *A, float *P, float *T, void *stream);
 
+/*
+ * kda_probe_wait_timeout -- test hook for the kernels' bounded pipeline waits.
+ * One CTA whose two waiting lanes each wait on a shared-memory mbarrier that
+ * nothing ever arrives on, through the same slow wait path as the forward
+ * kernels, giving up after `polls` polls (1 .. 2^18; each poll suspends the
+ * thread for at most 20 us). The first wait to give up sets
+ * KDA_ERR_DEVICE's timeout bit in the device error word (read and cleared
+ * by kda_check_device_status) and the CTA's abort flag, which ends the other
+ * wait. `result` (DEVICE int[3], written): result[0], result[1] = 1 if that
+ * wait succeeded (never expected), result[2] = the abort flag (1 expected).
+ * No copy or other work is in flight when the waits give up, so the kernel
+ * returns normally and the context stays usable. The pages have no
+ * counterpart: this checks the build's own failure path. Asynchronous on
+ * `stream`; KDA_ERR_NULL for a NULL result, KDA_ERR_RANGE for `polls`
+ * outside its range, KDA_ERR_LAUNCH for a failed launch.
+ */
+KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream);
+
 /* gate_scale = lower_bound * log2(e), rounded to float, exactly as the kernel
  * receives it [LB "Conversion to the Gate Scale Factor"]. Host only. */
 KDA_API float kda_gate_scale(float lower_bound);

@@ -155,6 +155,13 @@ def test_chunk32_flag_is_validated_on_the_host(kda):
         kda.fwd(*([None] * 7), chunk=64)
 
 
+def test_wait_timeout_probe_checks_its_arguments_on_the_host(kda):
+    lib = kda.library()
+    assert lib.kda_probe_wait_timeout(16, None, None) == 1  # KDA_ERR_NULL
+    assert lib.kda_probe_wait_timeout(0, 0x1000, None) == 4  # KDA_ERR_RANGE
+    assert lib.kda_probe_wait_timeout((1 << 18) + 1, 0x1000, None) == 4
+
+
 @pytest.mark.parametrize("value", ["3", "0", "16", "x"])
 def test_v_split_override_rejects_bad_values(kda, monkeypatch, value):
     monkeypatch.setenv("KDA_V_SPLIT", value)
