@@ -132,11 +132,11 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e =
-            cudaFuncSetAttribute(v1::kda_fwd_kernel<NS, QKN>, cudaFuncAttributeMaxDynamicSharedMemorySize, v1::SMEM_ALLOC);
+            cudaFuncSetAttribute(v1::kda_fwd_kernel<NS, QKN>, cudaFuncAttributeMaxDynamicSharedMemorySize, v1::Layout<NS>::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    v1::kda_fwd_kernel<NS, QKN><<<static_cast<unsigned>(grid), 32 * (1 + 2 * v1::NP + NS), v1::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    v1::kda_fwd_kernel<NS, QKN><<<static_cast<unsigned>(grid), v1::Layout<NS>::NTHREADS, v1::Layout<NS>::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
 }
 

@@ -9,9 +9,6 @@ namespace kda {
 namespace v1 {
 
 // ---------------------------------------------------------------- shared memory plan
-constexpr int NR = 6;                 // raw q/k/v/g ring depth (chunks)
-constexpr int NP = 3;                 // prep ring depth = number of prep lanes
-
 constexpr int BZ_LD = 272;            // row pitch (bytes) of 128-wide 16-bit tiles (136 elements)
 constexpr int SM_LD = 48;             // row pitch of 16x16 16-bit tiles (24 elements)
 constexpr int P_BZ = 0;                           // bf16 [32][136]: K*Gamma rows 0-15, Q*Gamma rows 16-31
@@ -22,28 +19,37 @@ constexpr int P_GAM = P_PP + 16 * SM_LD;          // f32  [128]:     gamma = Gam
 constexpr int PREP_SLOT = P_GAM + DH * 4;
 
 constexpr int H_LD = 272;             // row pitch of 16-bit [16][136] tiles
-constexpr int S_KLH = 0;              // bf16 hi/lo of K * 2^(G - G_mid), Q * 2^(G - G_mid), K * 2^(G_mid - G)
-constexpr int S_KLL = S_KLH + 16 * H_LD;
-constexpr int S_QLH = S_KLL + 16 * H_LD;
-constexpr int S_QLL = S_QLH + 16 * H_LD;
-constexpr int S_KRH = S_QLL + 16 * H_LD;
+constexpr int S_KLH = 0;              // bf16 K * 2^(G - G_mid)
+constexpr int S_QLH = S_KLH + 16 * H_LD;  // bf16 Q * 2^(G - G_mid)
+constexpr int S_KRH = S_QLH + 16 * H_LD;  // bf16 hi / lo of K * 2^(G_mid - G)
 constexpr int S_KRL = S_KRH + 16 * H_LD;
 constexpr int S_BETA = S_KRL + 16 * H_LD;
 constexpr int S_NRM = S_BETA + 64;    // f32 [2 warps][32]: row sums of squares of k (rows 0-15) and q (16-31)
 constexpr int SCR = S_NRM + 256;
 
-constexpr int OFF_RAW = 0;
-constexpr int OFF_PREP = OFF_RAW + NR * RAW_STAGE;
-constexpr int OFF_SCR = OFF_PREP + NP * PREP_SLOT;
-constexpr int OFF_BAR = OFF_SCR + NP * SCR;
-constexpr int NBAR = 2 * NR + 2 * NP;
-constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;
-constexpr int SMEM_USED = OFF_FLAGS + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // the ring base is rounded up to 1024 B (128B swizzle)
-
-static_assert(PREP_SLOT % 16 == 0 && SCR % 16 == 0 && OFF_PREP % 1024 == 0, "alignment");
-static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+// Rings by the number of scan warps NS (16 V rows each). With few rows per CTA the scan of a chunk
+// is short and the prep lanes pace the CTA: three lanes with two slots each, so a lane can prepare
+// its next chunk while the scan still reads its previous one (raw ring 5 deep). With 64 rows
+// (NS = 4) the scan takes longer: four lanes with one slot each (raw ring 6 deep).
+template <int NS>
+struct Layout {
+    static constexpr int NP = NS >= 4 ? 4 : 3;             // prep lanes
+    static constexpr int NSLOT = NS >= 4 ? NP : 2 * NP;    // prep slots; chunk n uses slot n % NSLOT
+    static constexpr int NR = NS >= 4 ? 6 : 5;             // raw q/k/v/g ring depth (chunks)
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_PREP = OFF_RAW + NR * RAW_STAGE;
+    static constexpr int OFF_SCR = OFF_PREP + NSLOT * PREP_SLOT;
+    static constexpr int OFF_BAR = OFF_SCR + NP * SCR;
+    static constexpr int NBAR = 2 * NR + 2 * NSLOT;
+    static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_USED = OFF_FLAGS + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // the ring base is rounded up to 1024 B (128B swizzle)
+    static constexpr int NTHREADS = 32 * (1 + 2 * NP + NS);
+    static_assert(NSLOT % NP == 0, "each slot belongs to one lane");
+    static_assert(PREP_SLOT % 16 == 0 && SCR % 16 == 0 && OFF_PREP % 1024 == 0, "alignment");
+    static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
 
 // L2 scale factor 1 / sqrt(sum x^2 + 1e-6) of k row `lane` (lanes 0-15) or q row `lane - 16`
 // (lanes 16-31) of a prep lane's chunk: each thread holds two channels of every row, a warp 64
@@ -76,10 +82,14 @@ __device__ __forceinline__ float qk_row_scale64(const uint32_t (&kw)[CHUNK], con
 
 // QKN: L2-normalise the q and k rows in the element-wise pass (KDA_FLAG_QK_L2NORM).
 template <int NS, bool QKN>
-__global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
+__global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
     kda_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
 {
+    using L = Layout<NS>;
+    constexpr int NP = L::NP, NSLOT = L::NSLOT, NR = L::NR;
+    constexpr int OFF_RAW = L::OFF_RAW, OFF_PREP = L::OFF_PREP, OFF_SCR = L::OFF_SCR, OFF_BAR = L::OFF_BAR,
+                  OFF_FLAGS = L::OFF_FLAGS;
     extern __shared__ uint8_t smem_dyn[];
     // align to 1024 B by pointer arithmetic on the shared array, so that accesses
     // through `smem` stay in the shared address space
@@ -93,14 +103,14 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
 
     volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
     const uint32_t raw_full = sb + OFF_BAR, raw_empty = raw_full + NR * 8;
-    const uint32_t prep_full = raw_empty + NR * 8, prep_empty = prep_full + NP * 8;
+    const uint32_t prep_full = raw_empty + NR * 8, prep_empty = prep_full + NSLOT * 8;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NR; ++i) {
             mbar_init(raw_full + 8 * i, 1);
             mbar_init(raw_empty + 8 * i, 1 + NS);
         }
-        for (int i = 0; i < NP; ++i) {
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(prep_full + 8 * i, 1);
             mbar_init(prep_empty + 8 * i, NS);
         }
@@ -151,7 +161,6 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
         const int lw = lt >> 5;                     // warp within the lane
         const uint32_t bar_id = 1 + ln;
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
-        const uint32_t pslot = sb + OFF_PREP + ln * PREP_SLOT;
         const int c0 = 2 * lt;                      // this thread's channels c0, c0 + 1
         float a_h = 1.f, bias0 = 0.f, bias1 = 0.f;
         if (p.A_log) a_h = ex2_approx(__ldg(p.A_log + h) * LOG2E);
@@ -165,7 +174,9 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
         for (int n = ln; n < nch; n += NP) {
             bool failed = false;  // this thread's waits gave up; OR-reduced at the end of the chunk
             const int rs = n % NR;
-            const uint32_t rph = (n / NR) & 1, pph = (n / NP) & 1;
+            const uint32_t rph = (n / NR) & 1, pph = (n / NSLOT) & 1;
+            const int ps = n % NSLOT;  // slot ln or ln + NP
+            const uint32_t pslot = sb + OFF_PREP + ps * PREP_SLOT;
             const int tok0 = sp.bos + n * CHUNK;
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
             float blogit = 0.f;
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
                     G1[r] = acc1;
                 }
             }
-            if (!wait_bar(prep_empty + 8 * ln, pph ^ 1, flags)) failed = true;
+            if (!wait_bar(prep_empty + 8 * ps, pph ^ 1, flags)) failed = true;
 
             const float Gm0 = G0[7], Gm1 = G1[7];  // mid-chunk reference halves the exponent range
             const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
                 }
             }
             const bool stop = named_bar_or(bar_id, 64, failed);
-            if (lt == 0) mbar_arrive(prep_full + 8 * ln);
+            if (lt == 0) mbar_arrive(prep_full + 8 * ps);
             if (stop) break;
         }
         return;
@@ -314,8 +325,8 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NP + NS), 1)
 
     const int mi = lane >> 3, ri = lane & 7;
     for (int n = 0; n < nch; ++n) {
-        const int ps = n % NP, rs = n % NR;
-        const uint32_t pph = (n / NP) & 1, rph = (n / NR) & 1;
+        const int ps = n % NSLOT, rs = n % NR;
+        const uint32_t pph = (n / NSLOT) & 1, rph = (n / NR) & 1;
         bool ok = wait_bar(prep_full + 8 * ps, pph, flags);
         ok = ok && wait_bar(raw_full + 8 * rs, rph, flags);
         if (!__all_sync(0xffffffffu, ok)) break;
