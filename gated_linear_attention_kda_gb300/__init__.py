@@ -21,11 +21,14 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libkda.so")
+# KDA_DEBUG_BUILD=1 loads the bounds-checked build of the same sources (libkda_debug.so), which
+# reports an out-of-bounds access through check_device_status instead of faulting
+DEBUG_BUILD = os.environ.get("KDA_DEBUG_BUILD", "") == "1"
+LIB_PATH = os.path.join(_PKG, "libkda_debug.so" if DEBUG_BUILD else "libkda.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        "libkda.so is not built; run `python gated_linear_attention_kda_gb300/_build.py` "
+        f"{os.path.basename(LIB_PATH)} is not built; run `python gated_linear_attention_kda_gb300/_build.py` "
         "(or __graft_entry__.build()) first")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -68,6 +71,10 @@ _lib.kda_probe_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _P, _P, _P, _P,
 _lib.kda_probe_chunk.restype = _I
 _lib.kda_probe_wait_timeout.argtypes = [_I, _P, _P]
 _lib.kda_probe_wait_timeout.restype = _I
+_lib.kda_probe_bounds.argtypes = [_P, _P]
+_lib.kda_probe_bounds.restype = _I
+_lib.kda_debug_build.argtypes = []
+_lib.kda_debug_build.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
 _lib.kda_check_device_status.argtypes = [_P]
 _lib.kda_check_device_status.restype = _I
@@ -290,6 +297,25 @@ def probe_wait_timeout(polls, device=None):
         st = _lib.kda_probe_wait_timeout(int(polls), _ptr(res), ctypes.c_void_p(stream))
     _raise(st)
     return [int(x) for x in res.cpu()]
+
+
+def probe_bounds(device=None):
+    """Test hook: run the bounds checks on a shared address and a global index that are out of
+    range, without accessing them (``kda_probe_bounds``). Returns [shared check passed, global
+    check passed]: [0, 0] in the bounds-checked build (which also flags the device error word),
+    [1, 1] in the product build."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    res = torch.full((2,), -1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = _lib.kda_probe_bounds(_ptr(res), ctypes.c_void_p(stream))
+    _raise(st)
+    return [int(x) for x in res.cpu()]
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the bounds-checked build (``KDA_DEBUG_BUILD=1``)."""
+    return bool(_lib.kda_debug_build())
 
 
 def fwd_host(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,

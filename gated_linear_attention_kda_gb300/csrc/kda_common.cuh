@@ -20,8 +20,6 @@ constexpr int OFF_Q = 0, OFF_K = RAW_TILE, OFF_V = 2 * RAW_TILE, OFF_G = 3 * RAW
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-enum : unsigned { DEVERR_SEQLENS = 1u, DEVERR_TIMEOUT = 2u };
-__device__ unsigned int g_dev_error;
 
 struct Params {
     const uint16_t *beta;
@@ -79,6 +77,12 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity)
         if (mbar_try_wait_sleep(bar, parity, WAIT_HINT_NS)) return;
     atomicOr(&g_dev_error, DEVERR_TIMEOUT);
 }
+
+// Sizes (elements) of the call's activation-shaped and state-shaped buffers, for the debug
+// build's bounds checks.
+__device__ __forceinline__ size_t tokhead_elems(const Params &p) { return static_cast<size_t>(p.total) * p.H; }
+__device__ __forceinline__ size_t out_elems(const Params &p) { return tokhead_elems(p) * DH; }
+__device__ __forceinline__ size_t state_elems(const Params &p) { return static_cast<size_t>(p.nseq) * p.H * DH * DH; }
 
 struct Span {
     int bos, len;

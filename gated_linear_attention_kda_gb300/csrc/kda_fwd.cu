@@ -529,6 +529,18 @@ KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream)
     return KDA_OK;
 }
 
+KDA_API int kda_debug_build(void) { return kDebugChecks ? 1 : 0; }
+
+KDA_API kda_status kda_probe_bounds(int *result, void *stream)
+{
+    t_last_error.clear();
+    if (!result) return fail(KDA_ERR_NULL, "kda_probe_bounds: result is required");
+    probe::kda_probe_bounds_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(result);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "probe launch failed: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}
+
 KDA_API kda_status kda_check_device_status(void *stream)
 {
     t_last_error.clear();
@@ -543,8 +555,9 @@ KDA_API kda_status kda_check_device_status(void *stream)
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "reading the device status failed: %s", cudaGetErrorString(e));
     if (word)
-        return fail(KDA_ERR_DEVICE, "device error word 0x%x:%s%s", word, (word & DEVERR_SEQLENS) ? " bad cu_seqlens" : "",
-                    (word & DEVERR_TIMEOUT) ? " pipeline wait timed out" : "");
+        return fail(KDA_ERR_DEVICE, "device error word 0x%x:%s%s%s", word, (word & DEVERR_SEQLENS) ? " bad cu_seqlens" : "",
+                    (word & DEVERR_TIMEOUT) ? " pipeline wait timed out" : "",
+                    (word & DEVERR_BOUNDS) ? " out-of-bounds access caught (debug build)" : "");
     return KDA_OK;
 }
 

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
     // through `smem` stay in the shared address space
     uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
-#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
+#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + (smem_checked((a), sizeof(T), sb) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x / p.vsplit, slice = blockIdx.x % p.vsplit;
     const int seq = unit / p.H, h = unit % p.H;
@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
             const int tok0 = sp.bos + n * CHUNK;
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
             float blogit = 0.f;
-            if (lw == 1 && lane < Lv)
-                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lane) * p.H + h)) << 16);
+            const size_t bi = static_cast<size_t>(tok0 + lane) * p.H + h;
+            if (lw == 1 && lane < Lv && gmem_ok(bi, 1, tokhead_elems(p)))
+                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + bi)) << 16);
             if (!wait_bar(raw_full + 8 * rs, rph, flags)) failed = true;
             const uint32_t raw = sb + OFF_RAW + rs * RAW_STAGE;
 
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
         for (int hh = 0; hh < 2; ++hh) {
             const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
             float x = 0.f, y = 0.f;
-            if (p.init) {
+            if (p.init && gmem_ok(e, 2, state_elems(p))) {
                 if (p.init_dtype == KDA_DTYPE_FP32) {
                     const float2 w = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.init) + e);
                     x = w.x;
@@ -391,7 +392,8 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = 8 * nt + 2 * t + (i & 1), vr = vr0 + g + 8 * (i >> 1);
-                if (r < Lv) p.out[(static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr] = f2bf_bits(p.scale * z[2 + nt][i]);
+                const size_t oi = (static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr;
+                if (r < Lv && gmem_ok(oi, 1, out_elems(p))) p.out[oi] = f2bf_bits(p.scale * z[2 + nt][i]);
             }
 
         // S = S Diag(gamma) + E Kbar
@@ -421,6 +423,7 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
+                if (!gmem_ok(e, 2, state_elems(p))) continue;
                 if (p.fin_dtype == KDA_DTYPE_FP32)
                     *reinterpret_cast<float2 *>(static_cast<float *>(p.fin) + e) = make_float2(S[nt][2 * hh], S[nt][2 * hh + 1]);
                 else

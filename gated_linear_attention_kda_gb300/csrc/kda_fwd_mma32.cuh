@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(32 * (1 + 4 * NP + NS), 1)
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
-#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
+#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + (smem_checked((a), sizeof(T), sb) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x / p.vsplit, slice = blockIdx.x % p.vsplit;
     const int seq = unit / p.H, h = unit % p.H;
@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(32 * (1 + 4 * NP + NS), 1)
             const int tok0 = sp.bos + n * C2;
             const int Lv = min(C2, sp.len - n * C2);
             float blogit = 0.f;
-            if (lt < C2 && lt < Lv)
-                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + static_cast<size_t>(tok0 + lt) * p.H + h)) << 16);
+            const size_t bi = static_cast<size_t>(tok0 + lt) * p.H + h;
+            if (lt < C2 && lt < Lv && gmem_ok(bi, 1, tokhead_elems(p)))
+                blogit = __uint_as_float(static_cast<uint32_t>(__ldg(p.beta + bi)) << 16);
             if (!wait_bar(qkg_full + 8 * qs, qph, flags)) failed = true;
             const uint32_t raw = sb + OFF_QKG + qs * QKG_STAGE + hf * QKG_HALF;
 
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(32 * (1 + 4 * NP + NS), 1)
         for (int hh = 0; hh < 2; ++hh) {
             const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
             float x = 0.f, y = 0.f;
-            if (p.init) {
+            if (p.init && gmem_ok(e, 2, state_elems(p))) {
                 if (p.init_dtype == KDA_DTYPE_FP32) {
                     const float2 w = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.init) + e);
                     x = w.x;
@@ -499,7 +500,8 @@ __global__ void __launch_bounds__(32 * (1 + 4 * NP + NS), 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = 8 * nt + 2 * t + (i & 1), vr = vr0 + g + 8 * (i >> 1);
-                if (r < Lv) p.out[(static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr] = f2bf_bits(p.scale * z[4 + nt][i]);
+                const size_t oi = (static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr;
+                if (r < Lv && gmem_ok(oi, 1, out_elems(p))) p.out[oi] = f2bf_bits(p.scale * z[4 + nt][i]);
             }
 
         // S = S Diag(gamma) + E Kbar
@@ -531,6 +533,7 @@ __global__ void __launch_bounds__(32 * (1 + 4 * NP + NS), 1)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const size_t e = st_base + static_cast<size_t>(vr0 + g + 8 * hh) * DH + 8 * nt + 2 * t;
+                if (!gmem_ok(e, 2, state_elems(p))) continue;
                 if (p.fin_dtype == KDA_DTYPE_FP32)
                     *reinterpret_cast<float2 *>(static_cast<float *>(p.fin) + e) = make_float2(S[nt][2 * hh], S[nt][2 * hh + 1]);
                 else

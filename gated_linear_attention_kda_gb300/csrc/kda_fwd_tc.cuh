@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
 // plain C++ shared-memory access at a 32-bit shared address (lets the compiler schedule it)
-#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + ((a) - sb)))
+#define SM_AT(T, a) (*reinterpret_cast<T *>(smem + (smem_checked((a), sizeof(T), sb) - sb)))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x % p.H;
     const int seq = (p.cu && p.nseq <= LPT_MAX_SEQS) ? lpt_sequence(p, blockIdx.x / p.H) : blockIdx.x / p.H;
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll 1
         for (int g4 = 0; g4 < 4; ++g4) {
             uint32_t r32[32], r16[16];
-            if (!p.init) {
+            if (!p.init || !gmem_ok(st_row + 32 * g4, 32, state_elems(p))) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r32[i] = 0u;
             } else if (p.init_dtype == KDA_DTYPE_FP32) {
@@ -469,11 +469,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int Lv = min(CHUNK, sp.len - k * CHUNK);
             if (Lv == CHUNK) {
 #pragma unroll
-                for (int r = 0; r < CHUNK; ++r) op[r * ostride] = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
+                for (int r = 0; r < CHUNK; ++r)
+                    if (gmem_ok(static_cast<size_t>(op - p.out) + r * ostride, 1, out_elems(p)))
+                        op[r * ostride] = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
             } else {
 #pragma unroll
                 for (int r = 0; r < CHUNK; ++r)
-                    if (r < Lv) op[r * ostride] = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
+                    if (r < Lv && gmem_ok(static_cast<size_t>(op - p.out) + r * ostride, 1, out_elems(p)))
+                        op[r * ostride] = static_cast<uint16_t>(o8[r >> 1] >> (16 * (r & 1)));
             }
             op += CHUNK * ostride;
         }
@@ -486,7 +489,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 uint32_t r32[32];
                 tc::ld32(lb + T_S + 32 * g4, r32);
                 tc::wait_ld();
-                if (p.fin_dtype == KDA_DTYPE_FP32) {
+                if (!gmem_ok(st_row + 32 * g4, 32, state_elems(p))) {
+                } else if (p.fin_dtype == KDA_DTYPE_FP32) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + st_row + 32 * g4);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
@@ -539,7 +543,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto beta_bits = [&](int n) -> uint32_t {
             if (lt >= CHUNK) return 0u;
             const int r = min(n * CHUNK + lt, sp.len - 1);
-            return __ldg(p.beta + static_cast<size_t>(sp.bos + r) * p.H + h);
+            const size_t idx = static_cast<size_t>(sp.bos + r) * p.H + h;
+            return gmem_ok(idx, 1, tokhead_elems(p)) ? __ldg(p.beta + idx) : 0u;
         };
         uint32_t bnext = ln < nch ? beta_bits(ln) : 0u;
         bool failed = false;  // sticky: a wait gave up; OR-reduced at the lane barriers

@@ -122,5 +122,16 @@ __global__ void __launch_bounds__(64) kda_probe_wait_kernel(int polls, int *resu
     if (threadIdx.x == 0) result[2] = abort_flag;
 }
 
+// The bounds checks themselves, with no access made: a shared address 16 bytes past the CTA's
+// shared memory and a global index one past the end of a buffer of 10 elements. In the debug
+// build both checks fail (result 0) and set DEVERR_BOUNDS; in the product build they compile to
+// `true` (result 1) and set nothing.
+__global__ void kda_probe_bounds_kernel(int *result)
+{
+    if (threadIdx.x != 0) return;
+    result[0] = smem_ok(dbg_smem_end() + 16, 4) ? 1 : 0;
+    result[1] = gmem_ok(10, 1, 10) ? 1 : 0;
+}
+
 }  // namespace probe
 }  // namespace kda

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "kda_debug.cuh"
+
 namespace kda {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -14,6 +16,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
+    if (!smem_ok(bar, 8)) return;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
@@ -24,11 +27,13 @@ __device__ __forceinline__ void fence_mbar_init()
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
+    if (!smem_ok(bar, 8)) return;
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
+    if (!smem_ok(bar, 8)) return;
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
                  "r"(bytes)
                  : "memory");
@@ -39,6 +44,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // phase completes), so waiting warps do not take issue slots.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
+    if (!smem_ok(bar, 8)) return false;
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
@@ -50,6 +56,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
+    if (!smem_ok(bar, 8)) return false;
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
@@ -69,6 +76,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m)
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int c0, int c1, int c2,
                                             uint32_t bar)
 {
+    // the box starts on a 16-byte boundary: 8 bf16 channels
+    if (!smem_ok(dst, 16) || !smem_ok(bar, 8) || !(kDebugChecks ? dbg_flag((c0 & 7) == 0) : true)) return;
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
@@ -170,6 +179,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // carry the memory clobbers) but does not fence ordinary shared-memory accesses.
 __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
+    if (!smem_ok_warp(a, 16)) {
+        r0 = r1 = r2 = r3 = 0u;
+        return;
+    }
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(a));
@@ -177,6 +190,10 @@ __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t &r0, uint32_t &r1, 
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
+    if (!smem_ok_warp(a, 16)) {
+        r0 = r1 = r2 = r3 = 0u;
+        return;
+    }
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(a));
@@ -186,6 +203,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t &r0, uint32_t &r1
 // matrix i, which receives column r of that matrix's m16n8-style fragment.
 __device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3)
 {
+    if (!smem_ok_warp(a, 16)) return;
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r0), "r"(r1),
                  "r"(r2), "r"(r3)
                  : "memory");
@@ -195,6 +213,7 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t a, uint32_t r0, uint32_t r1, 
 // receives row r of that matrix's m16n8-style fragment (the accumulator layout, packed to 16 bits).
 __device__ __forceinline__ void stsm_x4(uint32_t a, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3)
 {
+    if (!smem_ok_warp(a, 16)) return;
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r0), "r"(r1),
                  "r"(r2), "r"(r3)
                  : "memory");

@@ -127,6 +127,7 @@ __device__ __forceinline__ void commit_w(uint32_t bar)
 // 32 lanes (this warp's quarter) x 32 consecutive 32-bit columns
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
 {
+    tmem_check(taddr, 32);
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                  "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -139,6 +140,7 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
 }
 __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
 {
+    tmem_check(taddr, 32);
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                  "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
@@ -149,6 +151,7 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
 }
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
 {
+    tmem_check(taddr, 16);
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                  "%16};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
@@ -157,6 +160,7 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
 }
 __device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
 {
+    tmem_check(taddr, 8);
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");

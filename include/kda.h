@@ -301,6 +301,27 @@ KDA_API kda_status kda_probe_chunk(const void *q, const void *k, const void *g, 
  */
 KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream);
 
+/*
+ * kda_debug_build -- 1 in the bounds-checked build of the library
+ * (libkda_debug.so, compiled with KDA_DEBUG), 0 in the product build. In the
+ * checked build every shared-memory, tensor-memory, TMA and global access of
+ * the forward kernels is checked first; an access outside its buffer is
+ * skipped and sets the out-of-bounds bit of the device error word, reported
+ * as KDA_ERR_DEVICE by kda_check_device_status. Host only.
+ */
+KDA_API int kda_debug_build(void);
+
+/*
+ * kda_probe_bounds -- test hook for those checks, making no access: one
+ * thread checks a shared address 16 bytes past its CTA's shared memory and
+ * a global index one past the end of a 10-element buffer. `result` (DEVICE
+ * int[2], written): 1 where the check passed. Checked build: {0, 0} and the
+ * out-of-bounds bit set; product build: {1, 1} and nothing set. No
+ * counterpart on the pages. Asynchronous on `stream`; KDA_ERR_NULL for a NULL
+ * result, KDA_ERR_LAUNCH for a failed launch.
+ */
+KDA_API kda_status kda_probe_bounds(int *result, void *stream);
+
 /* gate_scale = lower_bound * log2(e), rounded to float, exactly as the kernel
  * receives it [LB "Conversion to the Gate Scale Factor"]. Host only. */
 KDA_API float kda_gate_scale(float lower_bound);

@@ -155,6 +155,19 @@ def test_chunk32_flag_is_validated_on_the_host(kda):
         kda.fwd(*([None] * 7), chunk=64)
 
 
+def test_bounds_checked_build_exports_every_declared_symbol(kda):
+    """libkda_debug.so (the same sources with KDA_DEBUG) builds and exports the whole ABI; it says
+    it is the checked build, the product library says it is not."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_kda_build_t", os.path.join(ROOT, "gated_linear_attention_kda_gb300", "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    lib = ctypes.CDLL(b.build_library(debug=True))
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"libkda_debug.so does not export {s}"
+    assert lib.kda_debug_build() == 1 and kda.library().kda_debug_build() == 0
+
+
 def test_wait_timeout_probe_checks_its_arguments_on_the_host(kda):
     lib = kda.library()
     assert lib.kda_probe_wait_timeout(16, None, None) == 1  # KDA_ERR_NULL
