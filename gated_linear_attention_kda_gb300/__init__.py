@@ -75,6 +75,10 @@ _lib.kda_probe_bounds.argtypes = [_P, _P]
 _lib.kda_probe_bounds.restype = _I
 _lib.kda_debug_build.argtypes = []
 _lib.kda_debug_build.restype = _I
+_lib.kda_probe_slots.argtypes = [_P, _P, _P, _P, _P, _F, _P, _P, _P, _F, ctypes.c_int64, _P, _I, _P]
+_lib.kda_probe_slots.restype = _I
+_lib.kda_probe_slot_bytes.argtypes = []
+_lib.kda_probe_slot_bytes.restype = _I
 _lib.kda_last_error.restype = ctypes.c_char_p
 _lib.kda_check_device_status.argtypes = [_P]
 _lib.kda_check_device_status.restype = _I
@@ -311,6 +315,29 @@ def probe_bounds(device=None):
         st = _lib.kda_probe_bounds(_ptr(res), ctypes.c_void_p(stream))
     _raise(st)
     return [int(x) for x in res.cpu()]
+
+
+def probe_slots(q, k, v, g, beta, scale, A_log=None, dt_bias=None, lower_bound=-5.0, nchunks=None):
+    """Test hook: one head of T tokens (``q, k, v, g`` bf16 [T, 128], ``beta`` bf16 [T], ``A_log``
+    fp32 [1] or None, ``dt_bias`` fp32 [128] or None; CUDA) through the tcgen05 kernel, returning
+    the prep slot of each of the first ``nchunks`` chunks as the tensor core reads it: uint8
+    [nchunks, kda_probe_slot_bytes()] (layout in include/kda.h), and the outputs [T, 128]."""
+    T = q.shape[0]
+    for name, t, shp in (("q", q, (T, 128)), ("k", k, (T, 128)), ("v", v, (T, 128)), ("g", g, (T, 128)),
+                         ("beta", beta, (T,))):
+        _check(name, t, torch.bfloat16, shp, True)
+    _check("A_log", A_log, torch.float32, (1,), True)
+    _check("dt_bias", dt_bias, torch.float32, (128,), True)
+    n = (T + 15) // 16 if nchunks is None else int(nchunks)
+    dump = torch.zeros((n, _lib.kda_probe_slot_bytes()), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = _lib.kda_probe_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                                  _ptr(A_log), _ptr(dt_bias), float(lower_bound), T, _ptr(dump), n,
+                                  ctypes.c_void_p(stream))
+    _raise(st)
+    return dump, out
 
 
 def debug_build() -> bool:

@@ -37,6 +37,8 @@ struct Params {
     int total;    // length of the flattened token axis (B * T)
     float scale;
     float half_gs;  // 0.5 * lower_bound * log2(e)
+    void *dump;       // slot-dump instance of the tcgen05 kernel only: finished prep slots of CTA 0
+    int dump_chunks;  // ... for chunks 0 .. dump_chunks - 1
 };
 
 // Bounded wait on an mbarrier phase. Each poll may suspend the thread for up

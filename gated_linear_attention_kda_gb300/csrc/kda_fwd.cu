@@ -140,7 +140,7 @@ static cudaError_t launch(int64_t grid, cudaStream_t s, const CUtensorMap &q, co
     return cudaGetLastError();
 }
 
-template <bool QKN>
+template <bool QKN, bool DUMP = false>
 static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
                              const CUtensorMap &v, const CUtensorMap &g, const Params &p)
 {
@@ -148,12 +148,12 @@ static cudaError_t launch_tc(int64_t grid, cudaStream_t s, const CUtensorMap &q,
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(tcs::kda_fwd_tc_kernel<QKN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             tcs::SMEM_ALLOC);
+        cudaError_t e = cudaFuncSetAttribute(tcs::kda_fwd_tc_kernel<QKN, DUMP>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, tcs::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    tcs::kda_fwd_tc_kernel<QKN><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, p);
+    tcs::kda_fwd_tc_kernel<QKN, DUMP><<<static_cast<unsigned>(grid), tcs::NTHREADS, tcs::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
 }
 
@@ -290,7 +290,7 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
                            void *out, const float *A_log, const float *dt_bias, float lower_bound,
                            const void *initial_state, kda_dtype initial_dtype, void *final_state, kda_dtype final_dtype,
                            const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
-                           uint32_t flags, void *stream, int split_vs)
+                           uint32_t flags, void *stream, int split_vs, void *dump = nullptr, int dump_chunks = 0)
 {
     t_last_error.clear();
     constexpr uint32_t known = KDA_FLAG_QK_L2NORM | KDA_FLAG_CHUNK32;
@@ -389,6 +389,8 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
     p.total = static_cast<int>(total);
     p.scale = scale;
     p.half_gs = 0.5f * kda_gate_scale(lower_bound);
+    p.dump = dump;
+    p.dump_chunks = dump_chunks;
     int vs;
     int64_t grid;
     plan(nseq * H, nsm, &vs, &grid);
@@ -397,7 +399,9 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
         grid = nseq * H * vs;
     }
     p.vsplit = vs;
-    if (flags & KDA_FLAG_CHUNK32)
+    if (dump)
+        ce = launch_tc<false, true>(grid, s, mq, mk, mv, mg, p);  // the per-step probe (split 1)
+    else if (flags & KDA_FLAG_CHUNK32)
         ce = launch_split32(vs, grid, s, mq, mk, mv, mg, p);
     else
         ce = (flags & KDA_FLAG_QK_L2NORM) ? launch_split<true>(vs, grid, s, mq, mk, mv, mg, p)
@@ -530,6 +534,22 @@ KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream)
 }
 
 KDA_API int kda_debug_build(void) { return kDebugChecks ? 1 : 0; }
+
+KDA_API int kda_probe_slot_bytes(void) { return tcs::SLOT; }
+
+KDA_API kda_status kda_probe_slots(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                   float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                                   int64_t T, void *dump, int nchunks, void *stream)
+{
+    t_last_error.clear();
+    if (!dump) return fail(KDA_ERR_NULL, "kda_probe_slots: dump is required");
+    if (T < 1 || nchunks < 1 || nchunks > (T + CHUNK - 1) / CHUNK)
+        return fail(KDA_ERR_SHAPE, "kda_probe_slots: need T >= 1 and 1 <= nchunks <= ceil(T / 16) (T=%lld nchunks=%d)",
+                    (long long)T, nchunks);
+    if (!aligned(dump, 16)) return fail(KDA_ERR_ALIGN, "kda_probe_slots: dump must be 16-byte aligned");
+    return fwd_impl(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, nullptr, KDA_DTYPE_NONE, nullptr,
+                    KDA_DTYPE_NONE, nullptr, 0, 1, T, 1, DH, DH, 0, stream, 1, dump, nchunks);
+}
 
 KDA_API kda_status kda_probe_bounds(int *result, void *stream)
 {

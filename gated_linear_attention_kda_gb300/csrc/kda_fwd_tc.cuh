@@ -202,7 +202,9 @@ __device__ __forceinline__ void qk_row_scales(const uint2 (&kw)[4], const uint2 
 }
 
 // QKN: L2-normalise the q and k rows in the element-wise pass (KDA_FLAG_QK_L2NORM).
-template <bool QKN>
+// DUMP: also copy each finished prep slot of CTA 0 (chunks below p.dump_chunks) to p.dump, byte
+// for byte, when it is handed to the tensor core (the per-step probe; the product never sets it).
+template <bool QKN, bool DUMP = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p)
@@ -871,6 +873,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               pack_f16(cf[nu + 1][0], cf[nu + 1][1]), pack_f16(cf[nu + 1][2], cf[nu + 1][3]));
             }
             tc::fence_async_smem();
+            if constexpr (DUMP) {
+                // the slot is complete here: the lane's Z', V, Kbar, gamma and H''^T (HRDY), and
+                // this warp's TM, Phi and (H Phi^T)^T
+                if (blockIdx.x == 0 && n < p.dump_chunks) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(smem + (sl - sb));
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.dump) + static_cast<size_t>(n) * SLOT);
+                    for (int i = lane; i < SLOT / 16; i += 32) dst[i] = src[i];
+                }
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar(B_FDONE + 2 * ln + xb));

@@ -322,6 +322,45 @@ KDA_API int kda_debug_build(void);
  */
 KDA_API kda_status kda_probe_bounds(int *result, void *stream);
 
+/*
+ * kda_probe_slots -- test hook: the per-step operands of the tcgen05 kernel
+ * itself. One head (B = H = 1) of T tokens (q, k, v, g bf16 [T, 1, 128],
+ * beta bf16 [T, 1], out bf16 [T, 1, 128], A_log one fp32 or NULL, dt_bias
+ * fp32 [128] or NULL; DEVICE; no states) runs through the tcgen05 kernel
+ * (one CTA holding the whole state), and the prep slot of each chunk
+ * n < nchunks is copied, as the tensor core reads it, to `dump` + n *
+ * kda_probe_slot_bytes() (DEVICE, 16-byte aligned, written). Slot layout
+ * (byte offsets; "cm16" = 8x8 core matrices of 16-bit values, K-major,
+ * 128 B between K blocks and 256 B between N blocks; "cm32" = 8x4 core
+ * matrices of fp32, 128 B between K blocks, 1024 B between N blocks;
+ * "sw128" = rows of 128 B, 16-byte chunk index XOR row mod 8, as TMA's
+ * 128-byte swizzle):
+ *     0  Z' bf16 [32 rows][128]: rows 0-15 K Gamma, 16-31 Q Gamma, both
+ *        times gamma of the previous chunk; two 64-column blocks of 4 KB,
+ *        sw128
+ *  8192  V f16 [16 tokens][128], two 64-column blocks of 2 KB, sw128
+ * 12288  Kbar f16 [16][128] = K 2^(G_end - G), same layout as V
+ * 16384  Phi fp32 [32][32] = [[-T', 0], [-s M, s I]], cm32
+ * 20480  TM f16 [32][16] = [T' ; s M], cm16 (T' = (I + A)^-1 diag(beta),
+ *        M = P T', s = scale)
+ * 21504  (H Phi^T)^T f16 [32][16] with H = Kbar_{n-1} [K Gamma ; Q Gamma]^T,
+ *        cm16 (chunk 0: not used by the kernel)
+ * 22528  H''^T f16 [32][16] with H'' = Kbar_{n-2} Diag(gamma_{n-1})
+ *        [K Gamma ; Q Gamma]^T, cm16 (chunks 0, 1: not used)
+ * 23552  gamma fp32 [128] = 2^(G_end)
+ * (G: the gate's in-chunk inclusive cumsum in log2 units; Gamma = 2^G.)
+ * No counterpart on the pages: it checks the kernel's own steps. Asynchronous
+ * on `stream`; argument checks and errors as kda_fwd, plus KDA_ERR_NULL for a
+ * NULL dump, KDA_ERR_SHAPE for nchunks outside 1..ceil(T / 16).
+ */
+KDA_API kda_status kda_probe_slots(const void *q, const void *k, const void *v, const void *g,
+                                   const void *beta, float scale, void *out,
+                                   const float *A_log, const float *dt_bias, float lower_bound,
+                                   int64_t T, void *dump, int nchunks, void *stream);
+
+/* Bytes of one dumped prep slot of kda_probe_slots. Host only. */
+KDA_API int kda_probe_slot_bytes(void);
+
 /* gate_scale = lower_bound * log2(e), rounded to float, exactly as the kernel
  * receives it [LB "Conversion to the Gate Scale Factor"]. Host only. */
 KDA_API float kda_gate_scale(float lower_bound);
