@@ -41,6 +41,7 @@
 //    Exponential Terms", "Efficient 16x16 Matrix Inversion".
 //  * tensor contract, states, varlen: "FlashKDA Input Tensor Shapes and
 //    DTypes ..." -- all sections.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -482,11 +483,28 @@ KDA_API kda_status kda_decode_ex(const void *q, const void *k, const void *v, co
     p.H = static_cast<int>(H);
     p.scale = scale;
     p.lower_bound = lower_bound;
-    const int64_t grid = S * H * (DH / dec::ROWS_PER_CTA);
+    // one contiguous range of state rows per warp; enough CTAs to fill every SM, but no fewer than
+    // eight rows per warp
+    int dev = 0, nsm = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "CUDA device query failed: %s", cudaGetErrorString(ce));
+    // resident CTAs per SM of the instance about to run (registers decide), queried once per device
+    static thread_local int occ_dev = -1, occ[2] = {0, 0};
+    if (occ_dev != dev) {
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[0], dec::kda_decode_kernel<false>, dec::THREADS, 0);
+        if (ce == cudaSuccess) ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], dec::kda_decode_kernel<true>, dec::THREADS, 0);
+        if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "occupancy query failed: %s", cudaGetErrorString(ce));
+        occ_dev = dev;
+    }
+    const int per_sm = std::max(1, occ[(flags & KDA_FLAG_QK_L2NORM) ? 1 : 0]);
+    const long long nrows = static_cast<long long>(S) * H * DH;
+    const long long rows_per_cta = 8LL * (dec::THREADS / 32);
+    const long long grid = std::min<long long>(static_cast<long long>(nsm) * per_sm, (nrows + rows_per_cta - 1) / rows_per_cta);
     if (flags & KDA_FLAG_QK_L2NORM)
-        dec::kda_decode_kernel<true><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+        dec::kda_decode_kernel<true><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p, nrows);
     else
-        dec::kda_decode_kernel<false><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+        dec::kda_decode_kernel<false><<<static_cast<unsigned>(grid), dec::THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p, nrows);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString(e));
     return KDA_OK;
