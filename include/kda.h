@@ -379,8 +379,10 @@ KDA_API const char *kda_last_error(void);
 
 /*
  * kda_check_device_status -- reads and clears the library's device error
- * word of the current device (bad cu_seqlens entries, or a pipeline wait that
- * hit its iteration limit) and synchronises `stream`. The word is shared by
+ * word of the current device (bad cu_seqlens entries, a pipeline wait that
+ * hit its iteration limit, or -- in the bounds-checked build, see
+ * kda_debug_build -- an access outside its buffer that was caught and
+ * skipped) and synchronises `stream`. The word is shared by
  * every call of this library on the device: it is exchanged with 0 by one
  * atomic operation on `stream`, so a flag set by any earlier call is reported
  * once, by the first check that runs after it, and a flag raised meanwhile by
