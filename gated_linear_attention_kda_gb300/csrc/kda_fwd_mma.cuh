@@ -203,13 +203,9 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
                     G1[r] = acc1;
                 }
             }
-            if (!wait_bar(prep_empty + 8 * ps, pph ^ 1, flags)) failed = true;
-
-            const float Gm0 = G0[7], Gm1 = G1[7];  // mid-chunk reference halves the exponent range
-            const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
-            const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
-            SM_AT(float2, pslot + P_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
-            // all raw loads first: stores below may alias them as far as the compiler knows
+            // all raw loads first: stores below may alias them as far as the compiler knows. With
+            // in-kernel q/k normalisation the row scales need only these tiles, so they are formed
+            // here, while the lane would otherwise wait for its slot
             uint32_t kwv[CHUNK], qwv[CHUNK];
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
@@ -218,6 +214,12 @@ __global__ void __launch_bounds__(Layout<NS>::NTHREADS, 1)
             }
             float fqk = 1.f;
             if constexpr (QKN) fqk = qk_row_scale64(kwv, qwv, lane, lw, smem + (scr + S_NRM - sb), bar_id);
+            if (!wait_bar(prep_empty + 8 * ps, pph ^ 1, flags)) failed = true;
+
+            const float Gm0 = G0[7], Gm1 = G1[7];  // mid-chunk reference halves the exponent range
+            const float sm0 = ex2_approx(-Gm0), sm1 = ex2_approx(-Gm1);
+            const float se0 = ex2_approx(G0[15] - Gm0), se1 = ex2_approx(G1[15] - Gm1);
+            SM_AT(float2, pslot + P_GAM + c0 * 4) = make_float2(ex2_approx(G0[15]), ex2_approx(G1[15]));
 #pragma unroll
             for (int r = 0; r < CHUNK; ++r) {
                 const uint32_t kw = kwv[r], qw = qwv[r];
