@@ -101,6 +101,9 @@ def _call(kda, **over):
     (dict(init=0x100000, init_dt=2, fin=0x100000 + 4096, fin_dt=2), 5),
     (dict(q=0x1008), 6), (dict(out=0x6002), 6), (dict(beta=0x5001), 6),
     (dict(init=0x8008, init_dt=2), 6), (dict(cu=0x7004, N=1), 6),
+    # the largest problems: a token axis of 2^31 - 32 or more, more than 2^20 heads, more than 2^28 states
+    (dict(B=1, T=(1 << 31) - 16), 2), (dict(B=2, T=(1 << 30)), 2), (dict(H=(1 << 20) + 1), 2),
+    (dict(B=1 << 20, T=1, H=1 << 9), 2),
 ])
 def test_host_validation_rejects(kda, over, code):
     assert _call(kda, **over) == code

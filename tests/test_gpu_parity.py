@@ -150,6 +150,17 @@ def test_varlen_small_with_empty_and_ragged_sequences(H):
     _check(d, final_dtype="bf16", heads=None if H < 8 else [0, 33, 79])
 
 
+@pytest.mark.parametrize("N", [64, 65])
+def test_varlen_many_sequences_both_orders(N):
+    """64 sequences take the longest-first CTA order of the whole-state kernel, 65 the plain order
+    (lengths 0..40, so empty, single-chunk and ragged sequences all occur); H = 3 gives 192 / 195
+    states, more than the SMs, so every state is one CTA."""
+    gen = torch.Generator().manual_seed(11 + N)
+    lens = torch.randint(0, 41, (N,), generator=gen).tolist()
+    d = W.make("varlen_n16_h32", lengths=lens, H=3)
+    _check(d, final_dtype="bf16")
+
+
 @pytest.mark.parametrize("H", [2, 80])
 def test_varlen_equals_separate_calls(H):
     lens = [19, 48, 3, 33]
