@@ -36,10 +36,11 @@ def test_checked_build_catches_an_out_of_range_index_without_the_access():
 
 
 def test_parity_suites_pass_through_the_checked_build():
-    """Every parity test except the full-size ones (their oracle time dominates), through
-    libkda_debug.so."""
+    """Every parity test except the full-size ones (their oracle time dominates), including the
+    per-step slot checks of the tcgen05 kernel, through libkda_debug.so."""
     r = _run(["-m", "pytest", "-q", "-x", "-m", "gpu", "-k", "not full", "-p", "no:cacheprovider",
-              "tests/test_gpu_parity.py", "tests/test_gpu_chunk32.py", "tests/test_gpu_failure_paths.py"], timeout=1800)
+              "tests/test_gpu_parity.py", "tests/test_gpu_chunk32.py", "tests/test_gpu_slot_steps.py",
+              "tests/test_gpu_failure_paths.py"], timeout=1800)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
     import re
     m = re.search(r"(\d+) passed", r.stdout)
