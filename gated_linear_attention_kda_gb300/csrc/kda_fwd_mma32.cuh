@@ -79,12 +79,14 @@ static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 // Fragment (Frag16) element (row g + 8 (i >> 1), col 8 nt + 2 t + (i & 1)) of the 16x16 block.
 __device__ __forceinline__ void frag_store(uint8_t *p, const Frag16 &f, int lane)
 {
+    if (!smem_ok(smem_u32(p + lane * 32), 32)) return;
     float4 *q = reinterpret_cast<float4 *>(p + lane * 32);
     q[0] = make_float4(f.c[0][0], f.c[0][1], f.c[0][2], f.c[0][3]);
     q[1] = make_float4(f.c[1][0], f.c[1][1], f.c[1][2], f.c[1][3]);
 }
 __device__ __forceinline__ void frag_load_add(const uint8_t *p, Frag16 &f, int lane)
 {
+    if (!smem_ok(smem_u32(p + lane * 32), 32)) return;
     const float4 *q = reinterpret_cast<const float4 *>(p + lane * 32);
     const float4 a = q[0], b = q[1];
     f.c[0][0] += a.x; f.c[0][1] += a.y; f.c[0][2] += a.z; f.c[0][3] += a.w;
@@ -123,7 +125,8 @@ __device__ __forceinline__ void store_block(uint8_t *tile, const Frag16 &f, int 
                 v0 = j <= r ? v0 : 0.f;
                 v1 = j + 1 <= r ? v1 : 0.f;
             }
-            *reinterpret_cast<uint32_t *>(tile + (ro + r) * LD32 + (co + j) * 2) = pack_f16(v0, v1);
+            uint8_t *dst = tile + (ro + r) * LD32 + (co + j) * 2;
+            if (smem_ok(smem_u32(dst), 4)) *reinterpret_cast<uint32_t *>(dst) = pack_f16(v0, v1);
         }
     }
 }
