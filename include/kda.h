@@ -37,7 +37,11 @@
  * are DEVICE pointers except where noted. kda_fwd allocates no device memory,
  * keeps no per-call state, never synchronises, and runs asynchronously on the
  * caller's stream. Inputs are never modified. `out` is written in place
- * [SHAPES "Gating Tensors and Output Buffer"].
+ * [SHAPES "Gating Tensors and Output Buffer"]. kda_fwd, kda_fwd_ex,
+ * kda_fwd_packed and kda_decode(_ex) can be captured into a CUDA graph once
+ * the same entry point has run eagerly on the device (the first call sets up
+ * per-device kernel attributes on the host); kda_fwd_host and
+ * kda_check_device_status synchronise and cannot.
  */
 #ifndef KDA_H
 #define KDA_H
