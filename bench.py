@@ -355,9 +355,9 @@ def copy_ceiling(h2d, d2h, dev):
     return res
 
 
-def run_launches(n, workload=None, T=None):
-    """Run ``n`` forward passes of a workload (default: the benchmark's; ``T`` shortens it) for
-    profilers."""
+def run_launches(n, workload=None, T=None, chunk=16):
+    """Run ``n`` forward passes of a workload (default: the benchmark's; ``T`` shortens it;
+    ``chunk`` 32 runs the 32-token-chunk kernel) for profilers."""
     import torch
 
     import gated_linear_attention_kda_gb300 as kda
@@ -371,9 +371,9 @@ def run_launches(n, workload=None, T=None):
     fin = torch.empty(nseq, d["q"].shape[2], 128, 128, dtype=sdt, device="cuda")
     for _ in range(n):
         kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
-                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], chunk=chunk)
     kda.check_device_status()
-    print(f"ran {n} launches of {name} (T={d['q'].shape[1]})")
+    print(f"ran {n} launches of {name} (T={d['q'].shape[1]}, chunk {chunk})")
 
 
 DECODE_B, DECODE_H = 128, 16   # 2048 fp32 states of 64 KiB: 134 MB, larger than L2
@@ -500,7 +500,7 @@ def main():
                     help="kernel-only timing with raw q/k normalised in the kernel (KDA_FLAG_QK_L2NORM)")
     args = ap.parse_args()
     if args.launches:
-        run_launches(args.launches, args.workload, args.T)
+        run_launches(args.launches, args.workload, args.T, args.chunk)
         return
     if args.decode:
         run_decode(args)
