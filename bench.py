@@ -355,9 +355,9 @@ def copy_ceiling(h2d, d2h, dev):
     return res
 
 
-def run_launches(n, workload=None, T=None, chunk=16):
+def run_launches(n, workload=None, T=None, chunk=16, workspace=False):
     """Run ``n`` forward passes of a workload (default: the benchmark's; ``T`` shortens it;
-    ``chunk`` 32 runs the 32-token-chunk kernel) for profilers."""
+    ``chunk`` 32 runs the 32-token-chunk kernel; ``workspace`` calls kda_fwd_ws) for profilers."""
     import torch
 
     import gated_linear_attention_kda_gb300 as kda
@@ -369,11 +369,16 @@ def run_launches(n, workload=None, T=None, chunk=16):
     sdt = torch.float32 if d["initial_state"] is None else d["initial_state"].dtype
     out = torch.empty_like(c["v"])
     fin = torch.empty(nseq, d["q"].shape[2], 128, 128, dtype=sdt, device="cuda")
+    ws = torch.empty(kda.workspace_bytes(nseq, d["q"].shape[2], chunk=chunk), dtype=torch.uint8, device="cuda")
     for _ in range(n):
-        kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
-                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], chunk=chunk)
+        args = (c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+        if workspace:
+            kda.fwd_ws(*args, chunk=chunk, workspace=ws)
+        else:
+            kda.fwd(*args, chunk=chunk)
     kda.check_device_status()
-    print(f"ran {n} launches of {name} (T={d['q'].shape[1]}, chunk {chunk})")
+    print(f"ran {n} launches of {name} (T={d['q'].shape[1]}, chunk {chunk}, workspace {workspace})")
 
 
 DECODE_B, DECODE_H = 128, 16   # 2048 fp32 states of 64 KiB: 134 MB, larger than L2
@@ -424,8 +429,9 @@ def run_decode(args):
 
 def run_variant(args):
     """Kernel-only timing of one workload (``--workload``, reshaped by ``--B/--T/--H``), optionally
-    with raw q/k normalised in the kernel (``--qk-norm``), 32-token chunks (``--chunk 32``) or a
-    forced split of the V rows (``--v-split``): its own JSON line, tokens/s and the HBM fraction of
+    with raw q/k normalised in the kernel (``--qk-norm``), 32-token chunks (``--chunk 32``), a
+    forced split of the V rows (``--v-split``) or through kda_fwd_ws with a workspace allocated
+    before the timed region (``--workspace``): its own JSON line, tokens/s and the HBM fraction of
     the algorithmic bytes. Not the benchmark line."""
     import torch
 
@@ -442,10 +448,16 @@ def run_variant(args):
     sdt = torch.float32 if d["initial_state"] is None else d["initial_state"].dtype
     out = torch.empty_like(c["v"])
     fin = torch.empty(nseq, H, 128, 128, dtype=sdt, device="cuda")
+    ws_bytes = kda.workspace_bytes(nseq, H, qk_l2norm=args.qk_norm, chunk=args.chunk) if args.workspace else 0
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
 
     def step():
-        kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
-                d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"], qk_l2norm=args.qk_norm, chunk=args.chunk)
+        a = (c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+             d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+        if args.workspace:
+            kda.fwd_ws(*a, qk_l2norm=args.qk_norm, chunk=args.chunk, workspace=ws)
+        else:
+            kda.fwd(*a, qk_l2norm=args.qk_norm, chunk=args.chunk)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -469,6 +481,8 @@ def run_variant(args):
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic", "config": {"workload": name, "B": B, "T": T, "H": H, "sequences": nseq,
                                         "qk_l2norm": bool(args.qk_norm), "chunk": args.chunk,
+                                        "entry": "kda_fwd_ws" if args.workspace else "kda_fwd",
+                                        "workspace_bytes": ws_bytes,
                                         "v_split": args.v_split or kda.plan(nseq * H, torch.cuda.get_device_properties(0).multi_processor_count)[0]},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": src, "algorithmic_bytes_per_launch": nbytes},
@@ -496,16 +510,18 @@ def main():
                     help="kernel-only timing with 32-token chunks (KDA_FLAG_CHUNK32, the chunk-size ablation)")
     ap.add_argument("--v-split", type=int, choices=[1, 2, 4, 8], default=None,
                     help="kernel-only timing with the V rows of each state split over this many CTAs (KDA_V_SPLIT)")
+    ap.add_argument("--workspace", action="store_true",
+                    help="kernel-only timing through kda_fwd_ws: a split state's CTAs share each chunk's preparation")
     ap.add_argument("--qk-norm", action="store_true",
                     help="kernel-only timing with raw q/k normalised in the kernel (KDA_FLAG_QK_L2NORM)")
     args = ap.parse_args()
     if args.launches:
-        run_launches(args.launches, args.workload, args.T, args.chunk)
+        run_launches(args.launches, args.workload, args.T, args.chunk, args.workspace)
         return
     if args.decode:
         run_decode(args)
         return
-    if args.workload or args.qk_norm or args.chunk != 16 or args.v_split or args.B or args.H or args.T:
+    if args.workload or args.qk_norm or args.chunk != 16 or args.v_split or args.B or args.H or args.T or args.workspace:
         run_variant(args)
         return
     if args.impl == "reference":

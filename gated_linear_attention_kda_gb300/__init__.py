@@ -49,6 +49,10 @@ _lib.kda_fwd_flat.restype = _I
 FWD_EX_ARGTYPES = FWD_ARGTYPES[:-1] + [ctypes.c_uint32, _P]
 _lib.kda_fwd_ex.argtypes = FWD_EX_ARGTYPES
 _lib.kda_fwd_ex.restype = _I
+_lib.kda_fwd_ws.argtypes = FWD_ARGTYPES[:-1] + [ctypes.c_uint32, _P, ctypes.c_size_t, _P]
+_lib.kda_fwd_ws.restype = _I
+_lib.kda_fwd_workspace_bytes.argtypes = [_I64, _I64, ctypes.c_uint32, ctypes.POINTER(ctypes.c_size_t)]
+_lib.kda_fwd_workspace_bytes.restype = _I
 
 
 class FwdArgs(ctypes.Structure):
@@ -198,6 +202,40 @@ def fwd(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0
             st = _lib.kda_fwd_ex(*args, flags, stream)
         else:
             st = _lib.kda_fwd(*args, stream)
+    _raise(st)
+    return out, final_state
+
+
+def workspace_bytes(states, H, qk_l2norm=False, chunk=16) -> int:
+    """Bytes of workspace ``fwd_ws`` uses for ``states`` sequences x ``H`` heads on the current
+    device (0 when the call's plan does not split the state)."""
+    n = ctypes.c_size_t(0)
+    _raise(_lib.kda_fwd_workspace_bytes(int(states), int(H), _flags(qk_l2norm, chunk), ctypes.byref(n)))
+    return int(n.value)
+
+
+def fwd_ws(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+           initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False, chunk=16, workspace=None):
+    """``fwd`` through ``kda_fwd_ws``: with a workspace of ``workspace_bytes`` bytes (a CUDA uint8
+    tensor), a split state's chunk preparation is shared by the CTAs of the state. Results equal
+    ``fwd``'s bit for bit."""
+    flags = _flags(qk_l2norm, chunk)
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=True)
+    nbytes = 0
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor")
+        _same_device(q.device, [("workspace", workspace)])
+        nbytes = workspace.numel()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+            _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+            _ptr(initial_state), _state_code(initial_state),
+            _ptr(final_state), _state_code(final_state),
+            _ptr(cu_seqlens), N, B, T, H, K, V)
+    with torch.cuda.device(q.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
+        st = _lib.kda_fwd_ws(*args, flags, _ptr(workspace), ctypes.c_size_t(nbytes), stream)
     _raise(st)
     return out, final_state
 

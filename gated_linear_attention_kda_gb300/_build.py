@@ -11,7 +11,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkda.so")
 DEBUG_LIB = os.path.join(PKG, "libkda_debug.so")  # the same sources with KDA_DEBUG bounds checks
 SOURCES = [os.path.join(CSRC, "kda_fwd.cu")]
-HEADERS = [os.path.join(CSRC, h) for h in ("kda_debug.cuh", "ptx.cuh", "kda_common.cuh", "kda_chunk.cuh", "kda_fwd_mma.cuh", "kda_fwd_mma32.cuh", "tcgen05.cuh", "kda_fwd_tc.cuh", "kda_probe.cuh", "kda_decode.cuh")] + [os.path.join(INCLUDE, "kda.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("kda_debug.cuh", "ptx.cuh", "kda_common.cuh", "kda_chunk.cuh", "kda_fwd_mma.cuh", "kda_fwd_mma32.cuh", "cluster.cuh", "kda_fwd_shared.cuh", "tcgen05.cuh", "kda_fwd_tc.cuh", "kda_probe.cuh", "kda_decode.cuh")] + [os.path.join(INCLUDE, "kda.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,6 +61,7 @@
 #include "kda_common.cuh"
 #include "kda_fwd_mma.cuh"
 #include "kda_fwd_mma32.cuh"
+#include "kda_fwd_shared.cuh"
 #include "kda_fwd_tc.cuh"
 #include "kda_probe.cuh"
 #include "kda_decode.cuh"
@@ -173,6 +174,79 @@ static cudaError_t launch32(int64_t grid, cudaStream_t s, const CUtensorMap &q, 
     }
     v32::kda_fwd32_kernel<NS><<<static_cast<unsigned>(grid), 32 * (1 + 4 * v32::NP + NS), v32::SMEM_ALLOC, s>>>(q, k, v, g, p);
     return cudaGetLastError();
+}
+
+// The split-state kernel with shared chunk preparation: one cluster of VS = 8 / NS CTAs per state,
+// the prepared operands handed between them through the workspace `ws`.
+template <int NS>
+static cudaLaunchConfig_t shared_config(int64_t grid, cudaStream_t s, cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(32 * (1 + 2 * v1s::NL + NS));
+    cfg.dynamicSmemBytes = v1s::SMEM_ALLOC;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 8 / NS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Clusters the device holds at once for this instance (0: cannot run), queried once per device.
+template <int NS>
+static int shared_capacity(int dev)
+{
+    static std::mutex mu;
+    static int cache[256];
+    static bool have[256] = {};
+    if (dev < 0 || dev >= 256) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        int n = 0;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = shared_config<NS>(8 / NS, nullptr, attr);
+        if (cudaFuncSetAttribute(v1s::kda_fwd_shared_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 v1s::SMEM_ALLOC) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, v1s::kda_fwd_shared_kernel<NS>, &cfg) != cudaSuccess)
+            n = 0;
+        cudaGetLastError();  // a refused query leaves no sticky error behind
+        cache[dev] = n;
+        have[dev] = true;
+    }
+    return cache[dev];
+}
+
+template <int NS>
+static cudaError_t launch_shared(int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
+                                 const CUtensorMap &v, const CUtensorMap &g, const Params &p, uint8_t *ws)
+{
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = shared_config<NS>(grid, s, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, v1s::kda_fwd_shared_kernel<NS>, q, k, v, g, p, ws);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+static int shared_capacity_for(int vs, int dev)
+{
+    switch (vs) {
+        case 2: return shared_capacity<4>(dev);
+        case 4: return shared_capacity<2>(dev);
+        case 8: return shared_capacity<1>(dev);
+        default: return 0;
+    }
+}
+
+static cudaError_t launch_split_shared(int vs, int64_t grid, cudaStream_t s, const CUtensorMap &q, const CUtensorMap &k,
+                                       const CUtensorMap &v, const CUtensorMap &g, const Params &p, uint8_t *ws)
+{
+    switch (vs) {
+        case 2: return launch_shared<4>(grid, s, q, k, v, g, p, ws);
+        case 4: return launch_shared<2>(grid, s, q, k, v, g, p, ws);
+        default: return launch_shared<1>(grid, s, q, k, v, g, p, ws);
+    }
 }
 
 // 32-token chunks (KDA_FLAG_CHUNK32): the warp-MMA kernel at every split, 128 / split V rows per CTA
@@ -291,7 +365,8 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
                            void *out, const float *A_log, const float *dt_bias, float lower_bound,
                            const void *initial_state, kda_dtype initial_dtype, void *final_state, kda_dtype final_dtype,
                            const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
-                           uint32_t flags, void *stream, int split_vs, void *dump = nullptr, int dump_chunks = 0)
+                           uint32_t flags, void *stream, int split_vs, void *dump = nullptr, int dump_chunks = 0,
+                           void *ws = nullptr, size_t ws_bytes = 0)
 {
     t_last_error.clear();
     constexpr uint32_t known = KDA_FLAG_QK_L2NORM | KDA_FLAG_CHUNK32;
@@ -400,8 +475,16 @@ static kda_status fwd_impl(const void *q, const void *k, const void *v, const vo
         grid = nseq * H * vs;
     }
     p.vsplit = vs;
+    // split states with a workspace: the chunk preparation is shared by a state's CTAs
+    const bool shared = ws && vs >= 2 && !dump && !(flags & (KDA_FLAG_CHUNK32 | KDA_FLAG_QK_L2NORM)) &&
+                        shared_capacity_for(vs, dev) > 0;
+    if (shared && static_cast<int64_t>(ws_bytes) < nseq * H * v1s::workspace_bytes_per_state())
+        return fail(KDA_ERR_RANGE, "workspace of %zu bytes is smaller than the %lld this call needs", ws_bytes,
+                    (long long)(nseq * H * v1s::workspace_bytes_per_state()));
     if (dump)
         ce = launch_tc<false, true>(grid, s, mq, mk, mv, mg, p);  // the per-step probe (split 1)
+    else if (shared)
+        ce = launch_split_shared(vs, grid, s, mq, mk, mv, mg, p, static_cast<uint8_t *>(ws));
     else if (flags & KDA_FLAG_CHUNK32)
         ce = launch_split32(vs, grid, s, mq, mk, mv, mg, p);
     else
@@ -552,6 +635,41 @@ KDA_API kda_status kda_probe_wait_timeout(int polls, int *result, void *stream)
 }
 
 KDA_API int kda_debug_build(void) { return kDebugChecks ? 1 : 0; }
+
+KDA_API kda_status kda_fwd_workspace_bytes(int64_t states, int64_t H, uint32_t flags, size_t *bytes)
+{
+    t_last_error.clear();
+    if (!bytes) return fail(KDA_ERR_NULL, "kda_fwd_workspace_bytes: bytes is required");
+    if (states < 0 || H < 1) return fail(KDA_ERR_SHAPE, "bad sizes states=%lld H=%lld", (long long)states, (long long)H);
+    int dev = 0, nsm = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (ce != cudaSuccess) return fail(KDA_ERR_LAUNCH, "CUDA device query failed: %s", cudaGetErrorString(ce));
+    int vs;
+    int64_t grid;
+    plan(states * H, nsm, &vs, &grid);
+    if (const char *env = std::getenv("KDA_V_SPLIT")) {
+        const int f = std::atoi(env);
+        if (f == 1 || f == 2 || f == 4 || f == 8) vs = f;
+    }
+    const bool shared =
+        vs >= 2 && !(flags & (KDA_FLAG_CHUNK32 | KDA_FLAG_QK_L2NORM)) && shared_capacity_for(vs, dev) > 0;
+    *bytes = shared ? static_cast<size_t>(states * H * v1s::workspace_bytes_per_state()) : 0;
+    return KDA_OK;
+}
+
+KDA_API kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                              void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                              const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                              kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                              int64_t H, int64_t K, int64_t V, uint32_t flags, void *workspace, size_t workspace_bytes,
+                              void *stream)
+{
+    t_last_error.clear();
+    if (workspace && !aligned(workspace, 16)) return fail(KDA_ERR_ALIGN, "workspace must be 16-byte aligned");
+    return fwd_impl(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype, final_state,
+                    final_dtype, cu_seqlens, N, B, T, H, K, V, flags, stream, 0, nullptr, 0, workspace, workspace_bytes);
+}
 
 KDA_API int kda_probe_slot_bytes(void) { return tcs::SLOT; }
 

@@ -46,6 +46,7 @@
 #ifndef KDA_H
 #define KDA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -178,6 +179,48 @@ KDA_API kda_status kda_fwd_ex(const void *q, const void *k, const void *v, const
                               const int64_t *cu_seqlens, int64_t N,
                               int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
                               uint32_t flags, void *stream);
+
+/*
+ * kda_fwd_ws -- kda_fwd_ex with a caller-owned DEVICE workspace that lets the
+ * CTAs of a split state share the chunk preparation [CHUNK "Algorithm
+ * Overview": gate, cumsum, intra-chunk matrices and their inverse, made once per
+ * chunk]. When the plan splits a state's V rows across 2, 4 or 8 CTAs (kda_plan
+ * or KDA_V_SPLIT) and flags == 0, those CTAs run as one thread-block cluster:
+ * each prepares one chunk in `split`, publishes the prepared operands to
+ * `workspace`, and reads the others' back through L2. Results equal kda_fwd_ex's
+ * bit for bit.
+ *   workspace        16-byte aligned device buffer of at least the
+ *                    kda_fwd_workspace_bytes bytes for (N or B) x H states;
+ *                    NULL (or a call that does not split, or any flag set, or
+ *                    a device that cannot hold one cluster of the split's
+ *                    size) runs kda_fwd_ex's kernels.
+ *                    The contents need no initialisation and are scratch
+ *                    after the call; calls that overlap in time must not share
+ *                    a workspace.
+ *   workspace_bytes  its size; smaller than needed is KDA_ERR_RANGE,
+ *                    misaligned KDA_ERR_ALIGN.
+ * Every other argument, check and error is kda_fwd_ex's. The library
+ * allocates nothing.
+ */
+KDA_API kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, float scale, void *out,
+                              const float *A_log, const float *dt_bias, float lower_bound,
+                              const void *initial_state, kda_dtype initial_dtype,
+                              void *final_state, kda_dtype final_dtype,
+                              const int64_t *cu_seqlens, int64_t N,
+                              int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                              uint32_t flags, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * kda_fwd_workspace_bytes -- the workspace kda_fwd_ws needs for `states`
+ * sequences (N in varlen mode, else B) of H heads with option bits `flags` on
+ * the current device: states x H x 16 prepared chunks of 15104 bytes when
+ * kda_fwd_ws would share the preparation (the plan splits the state, no flag
+ * is set and the device holds a cluster of the split's size), else 0. Needs a CUDA device (it reads the SM count);
+ * KDA_ERR_NULL for a NULL `bytes`, KDA_ERR_SHAPE for states < 0 or H < 1.
+ */
+KDA_API kda_status kda_fwd_workspace_bytes(int64_t states, int64_t H, uint32_t flags, size_t *bytes);
 
 /*
  * kda_fwd_args / kda_fwd_packed -- the same operation with its arguments in

@@ -27,7 +27,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     assert {"kda_fwd", "kda_fwd_flat", "kda_fwd_packed", "kda_fwd_host", "kda_fwd_ex", "kda_decode",
             "kda_decode_ex", "kda_check_device_status", "kda_last_error", "kda_plan", "kda_gate_scale",
-            "kda_version"} <= set(syms)
+            "kda_version", "kda_fwd_ws", "kda_fwd_workspace_bytes"} <= set(syms)
 
 
 def test_library_exports_every_declared_symbol(kda):
@@ -256,3 +256,19 @@ def test_host_entry_checks_its_host_cu_seqlens_before_any_copy(kda):
                               cu.ctypes.data_as(ctypes.c_void_p), len(bad) - 1, 1, 8, 2, 128, 128, None)
         assert st == 2, bad  # KDA_ERR_SHAPE
         assert b"cu_seqlens" in lib.kda_last_error()
+
+
+def test_workspace_entry_points_validate_on_the_host(kda):
+    """kda_fwd_ws checks its workspace's alignment and then every argument as kda_fwd_ex does;
+    kda_fwd_workspace_bytes rejects a NULL result pointer and bad sizes. No GPU is touched."""
+    lib = kda.library()
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0, None, 0, 1, 16, 1)
+    assert lib.kda_fwd_ws(*args, 128, 128, 0, 0x7001, 1 << 20, None) == 6  # misaligned workspace: KDA_ERR_ALIGN
+    assert b"workspace" in lib.kda_last_error()
+    assert lib.kda_fwd_ws(*args, 64, 128, 0, 0x7000, 1 << 20, None) == 2  # K != 128: KDA_ERR_SHAPE
+    assert lib.kda_fwd_ws(*args, 128, 128, 4, 0x7000, 1 << 20, None) == 4  # unknown option bit: KDA_ERR_RANGE
+    assert lib.kda_fwd_workspace_bytes(1, 1, 0, None) == 1
+    n = ctypes.c_size_t(7)
+    assert lib.kda_fwd_workspace_bytes(-1, 1, 0, ctypes.byref(n)) == 2
+    assert lib.kda_fwd_workspace_bytes(1, 0, 0, ctypes.byref(n)) == 2
+    assert n.value == 7  # untouched on error
