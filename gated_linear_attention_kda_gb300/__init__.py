@@ -53,6 +53,9 @@ _lib.kda_fwd_ws.argtypes = FWD_ARGTYPES[:-1] + [ctypes.c_uint32, _P, ctypes.c_si
 _lib.kda_fwd_ws.restype = _I
 _lib.kda_fwd_workspace_bytes.argtypes = [_I64, _I64, ctypes.c_uint32, ctypes.POINTER(ctypes.c_size_t)]
 _lib.kda_fwd_workspace_bytes.restype = _I
+_lib.kda_fwd_static.argtypes = FWD_EX_ARGTYPES
+_lib.kda_fwd_static.restype = _I
+STATIC_SCRATCH_STATES = 80  # KDA_STATIC_SCRATCH_STATES
 
 
 class FwdArgs(ctypes.Structure):
@@ -236,6 +239,26 @@ def fwd_ws(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-
     with torch.cuda.device(q.device):
         stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
         st = _lib.kda_fwd_ws(*args, flags, _ptr(workspace), ctypes.c_size_t(nbytes), stream)
+    _raise(st)
+    return out, final_state
+
+
+def fwd_static(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=-5.0,
+               initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False, chunk=16):
+    """``fwd`` through ``kda_fwd_static``: the shared chunk preparation of ``fwd_ws`` with the
+    library's own scratch (room for ``STATIC_SCRATCH_STATES`` states, no allocation). Calls that
+    overlap in time on one device share that scratch: issue them on one stream."""
+    flags = _flags(qk_l2norm, chunk)
+    B, T, H, K, V, N = _validate(q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state,
+                                 cu_seqlens, cuda=True)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+            _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+            _ptr(initial_state), _state_code(initial_state),
+            _ptr(final_state), _state_code(final_state),
+            _ptr(cu_seqlens), N, B, T, H, K, V)
+    with torch.cuda.device(q.device):
+        stream = ctypes.c_void_p(torch.cuda.current_stream(q.device).cuda_stream)
+        st = _lib.kda_fwd_static(*args, flags, stream)
     _raise(st)
     return out, final_state
 

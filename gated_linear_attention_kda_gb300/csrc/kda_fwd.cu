@@ -671,6 +671,63 @@ KDA_API kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const
                     final_dtype, cu_seqlens, N, B, T, H, K, V, flags, stream, 0, nullptr, 0, workspace, workspace_bytes);
 }
 
+// ---------------------------------------------------------------------------------------------
+// kda_fwd_static: kda_fwd_ws with a scratch array of the library's own (no allocation per call).
+// Room for KDA_STATIC_SCRATCH_STATES states: the plan splits a state only when states x 2 fit on
+// the SMs, at most 76 on a 152-SM GB300.
+static __device__ __align__(256) uint8_t g_static_scratch[KDA_STATIC_SCRATCH_STATES * 16 * v1s::PREP_SLOT];
+static_assert(KDA_STATIC_SCRATCH_STATES * 16 * v1s::PREP_SLOT == KDA_STATIC_SCRATCH_STATES * v1s::workspace_bytes_per_state(),
+              "the static scratch holds KDA_STATIC_SCRATCH_STATES workspaces");
+
+// The scratch array's device address on the current device, looked up once per device.
+static kda_status static_scratch(void **ptr)
+{
+    static std::mutex mu;
+    static void *addr[256];
+    static bool have[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "CUDA device query failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 256) return fail(KDA_ERR_LAUNCH, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
+        if (e != cudaSuccess) return fail(KDA_ERR_LAUNCH, "static scratch lookup failed: %s", cudaGetErrorString(e));
+        have[dev] = true;
+    }
+    *ptr = addr[dev];
+    return KDA_OK;
+}
+
+KDA_API kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                  float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                                  const void *initial_state, kda_dtype initial_dtype, void *final_state,
+                                  kda_dtype final_dtype, const int64_t *cu_seqlens, int64_t N, int64_t B, int64_t T,
+                                  int64_t H, int64_t K, int64_t V, uint32_t flags, void *stream)
+{
+    t_last_error.clear();
+    const int64_t nseq = cu_seqlens ? N : B;
+    const bool sizes_ok = K == DH && V == DH && B >= 1 && T >= 0 && H >= 1 && H <= (1 << 20) &&
+                          (!cu_seqlens || (B == 1 && N >= 1)) && nseq * H <= (int64_t(1) << 28);
+    size_t need = 0;
+    if (sizes_ok && B * T > 0 && kda_fwd_workspace_bytes(nseq, H, flags, &need) == KDA_OK && need > 0) {
+        if (need > sizeof(g_static_scratch))
+            return fail(KDA_ERR_RANGE,
+                        "kda_fwd_static: %lld states need %zu bytes of scratch; the static scratch holds %d states "
+                        "(%zu bytes): use kda_fwd_ws with a workspace",
+                        (long long)(nseq * H), need, KDA_STATIC_SCRATCH_STATES, sizeof(g_static_scratch));
+        void *ws = nullptr;
+        if (const kda_status st = static_scratch(&ws); st != KDA_OK) return st;
+        return fwd_impl(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype,
+                        final_state, final_dtype, cu_seqlens, N, B, T, H, K, V, flags, stream, 0, nullptr, 0, ws,
+                        sizeof(g_static_scratch));
+    }
+    // no scratch needed (or an argument error, reported as kda_fwd_ex reports it)
+    t_last_error.clear();
+    return fwd_impl(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, initial_dtype, final_state,
+                    final_dtype, cu_seqlens, N, B, T, H, K, V, flags, stream, 0, nullptr, 0, nullptr, 0);
+}
+
 KDA_API int kda_probe_slot_bytes(void) { return tcs::SLOT; }
 
 KDA_API kda_status kda_probe_slots(const void *q, const void *k, const void *v, const void *g, const void *beta,

@@ -223,6 +223,39 @@ KDA_API kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const
 KDA_API kda_status kda_fwd_workspace_bytes(int64_t states, int64_t H, uint32_t flags, size_t *bytes);
 
 /*
+ * kda_fwd_static -- kda_fwd_ws with the library's own scratch instead of a
+ * caller's workspace. The pages have no counterpart: it exists so that a
+ * caller who cannot hand over device memory still gets the shared chunk
+ * preparation, without any allocation. Arguments, checks and errors are
+ * kda_fwd_ex's, plus:
+ *   - the scratch is one file-scope device array of KDA_STATIC_SCRATCH_STATES
+ *     workspaces (KDA_STATIC_SCRATCH_STATES x 16 x 15104 bytes = 18.4 MiB),
+ *     part of the library's device image: no call allocates, frees or calls
+ *     an allocating library function;
+ *   - a call that would share the preparation for more than
+ *     KDA_STATIC_SCRATCH_STATES (N or B) x H states is KDA_ERR_RANGE, with a
+ *     message naming the limit; a call whose plan does not split the state
+ *     (or with option bits set) uses no scratch and has no limit;
+ *   - nothing in the scratch needs to start at zero: every entry is written
+ *     before it is read within a call;
+ *   - the first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) and sets the kernel attributes on the
+ *     host; later calls reuse them;
+ *   - calls that overlap in time on one device (on different streams, or
+ *     from several host threads) share the scratch and race: serialise them,
+ *     for example by issuing them on one stream.
+ */
+#define KDA_STATIC_SCRATCH_STATES 80
+KDA_API kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, float scale, void *out,
+                                  const float *A_log, const float *dt_bias, float lower_bound,
+                                  const void *initial_state, kda_dtype initial_dtype,
+                                  void *final_state, kda_dtype final_dtype,
+                                  const int64_t *cu_seqlens, int64_t N,
+                                  int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                                  uint32_t flags, void *stream);
+
+/*
  * kda_fwd_args / kda_fwd_packed -- the same operation with its arguments in
  * one struct. Every field has the meaning, layout and ownership of the
  * kda_fwd argument of the same name; the struct itself is read during the

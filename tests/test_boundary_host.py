@@ -27,7 +27,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     assert {"kda_fwd", "kda_fwd_flat", "kda_fwd_packed", "kda_fwd_host", "kda_fwd_ex", "kda_decode",
             "kda_decode_ex", "kda_check_device_status", "kda_last_error", "kda_plan", "kda_gate_scale",
-            "kda_version", "kda_fwd_ws", "kda_fwd_workspace_bytes"} <= set(syms)
+            "kda_version", "kda_fwd_ws", "kda_fwd_workspace_bytes", "kda_fwd_static"} <= set(syms)
 
 
 def test_library_exports_every_declared_symbol(kda):
@@ -272,3 +272,17 @@ def test_workspace_entry_points_validate_on_the_host(kda):
     assert lib.kda_fwd_workspace_bytes(-1, 1, 0, ctypes.byref(n)) == 2
     assert lib.kda_fwd_workspace_bytes(1, 0, 0, ctypes.byref(n)) == 2
     assert n.value == 7  # untouched on error
+
+
+def test_static_entry_point_validates_like_fwd_ex(kda):
+    """kda_fwd_static reports argument errors exactly as kda_fwd_ex does (no GPU touched), and
+    its scratch limit matches the header's."""
+    lib = kda.library()
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -5.0, None, 0, None, 0, None, 0, 1, 16, 1)
+    assert lib.kda_fwd_static(*args, 64, 128, 0, None) == 2  # K != 128: KDA_ERR_SHAPE
+    assert lib.kda_fwd_static(*args, 128, 128, 4, None) == 4  # unknown option bit: KDA_ERR_RANGE
+    assert b"option bits" in lib.kda_last_error()
+    assert lib.kda_fwd_static(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1.0, 0x6000, None, None, -6.0, None, 0, None,
+                              0, None, 0, 1, 16, 1, 128, 128, 0, None) == 4  # lower_bound outside [-5, 0]
+    hdr = open(HEADER).read()
+    assert re.search(r"#define KDA_STATIC_SCRATCH_STATES (\d+)", hdr).group(1) == str(kda.STATIC_SCRATCH_STATES)
