@@ -14,10 +14,10 @@
 //           chunk (mbarrier `gfree[e]` of the owner, one arrival per CTA): copy the slot to entry
 //           e, fence, and arrive on `ready[e]` of every CTA (release at cluster scope).
 //   all     the feeder thread waits for `ready[e]` (acquire at cluster scope) and bulk-copies
-//           entry e into an import slot; when it reuses that slot NI chunks later (the copy has
-//           long landed and been scanned), it releases entry e on the owner's `gfree[e]`. The
-//           feeder makes no generic stores, so its release costs nothing, and the scan warps,
-//           which do, never signal another CTA.
+//           entry e into a stage beside the chunk's V tile; when it reuses that stage NST chunks
+//           later (the copy has long landed and been scanned), it releases entry e on the owner's
+//           `gfree[e]`. The feeder makes no generic stores, so its signal waits for none, and
+//           the scan warps, which do, never signal another CTA.
 // The imported bytes are the prep lane's, so results equal the warp-MMA kernel's at the same
 // split bit for bit. The rows of S are independent, which is what makes the split exact
 // ("FlashKDA Input Tensor Shapes and DTypes ..." -- "Initial and Final States").
@@ -53,27 +53,32 @@ using v1::SM_LD;
 
 constexpr int NG = 16;  // workspace ring entries per state (an even multiple of every split)
 constexpr int NL = 2;   // prep lanes (own chunks alternate between them)
-constexpr int NI = 7;   // import slots
-constexpr int NV = 8;   // V ring depth
+constexpr int NST = 7;  // stages: the V tile and the imported prepared operands of one chunk
 
 constexpr int QKG_STAGE = 3 * RAW_TILE;  // q, k, g tiles of one chunk: one stage per prep lane
 constexpr int QS_Q = 0, QS_K = RAW_TILE, QS_G = 2 * RAW_TILE;
-constexpr int OFF_V = 0;
-constexpr int OFF_QKG = OFF_V + NV * RAW_TILE;
+constexpr int SLOT_PAD = (PREP_SLOT + 1023) / 1024 * 1024;
+constexpr int STAGE = RAW_TILE + SLOT_PAD;  // V tile (128B-swizzled, at a 1024-byte boundary), then the slot
+constexpr int OT_LD = 48;                   // row pitch of a scan warp's 16 x 16 bf16 output tile
+constexpr int OT_BYTES = 16 * OT_LD;
+constexpr int MAX_NS = 4;
+constexpr int OFF_STG = 0;
+constexpr int OFF_QKG = OFF_STG + NST * STAGE;
 constexpr int OFF_OWN = OFF_QKG + NL * QKG_STAGE;  // one staging slot per prep lane
-constexpr int OFF_IMP = OFF_OWN + NL * PREP_SLOT;
-constexpr int OFF_SCR = OFF_IMP + NI * PREP_SLOT;
-constexpr int OFF_BAR = OFF_SCR + NL * SCR;
-// barriers: V full / empty [NV], q/k/g full [NL], import full / empty [NI], ready [NG], gfree [NG]
-constexpr int NBAR = 2 * NV + NL + 2 * NI + 2 * NG;
+constexpr int OFF_SCR = OFF_OWN + NL * PREP_SLOT;
+constexpr int OFF_OT = OFF_SCR + NL * SCR;
+constexpr int OFF_BAR = OFF_OT + MAX_NS * OT_BYTES;
+// barriers: stage full / empty [NST], q/k/g full [NL], ready [NG], gfree [NG]
+constexpr int NBAR = 2 * NST + NL + 2 * NG;
 constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;
 constexpr int SMEM_USED = OFF_FLAGS + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // the ring base is rounded up to 1024 B (128B swizzle)
 
-static_assert(PREP_SLOT % 16 == 0 && OFF_IMP % 16 == 0 && OFF_OWN % 16 == 0, "bulk copies need 16-byte units");
+static_assert(PREP_SLOT % 16 == 0 && STAGE % 1024 == 0 && OFF_OWN % 16 == 0 && OFF_OT % 16 == 0,
+              "bulk copies and 16-byte accesses need 16-byte units");
 static_assert(RAW_TILE % 1024 == 0 && OFF_QKG % 1024 == 0, "128B-swizzled TMA boxes need 1024-byte alignment");
 static_assert(NG % 16 == 0, "a workspace entry keeps one owner and one prep lane at every split");
-static_assert(NG > NI, "an entry is released before its owner needs it again");
+static_assert(NG > NST, "an entry is released before its owner needs it again");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -99,21 +104,16 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
     uint8_t *wsu = ws + static_cast<size_t>(unit) * NG * PREP_SLOT;  // this state's workspace ring
 
     volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
-    const uint32_t v_full = sb + OFF_BAR, v_empty = v_full + NV * 8;
-    const uint32_t qkg_full = v_empty + NV * 8;
-    const uint32_t imp_full = qkg_full + NL * 8, imp_empty = imp_full + NI * 8;
-    const uint32_t ready = imp_empty + NI * 8, gfree = ready + NG * 8;
+    const uint32_t st_full = sb + OFF_BAR, st_empty = st_full + NST * 8;
+    const uint32_t qkg_full = st_empty + NST * 8;
+    const uint32_t ready = qkg_full + NL * 8, gfree = ready + NG * 8;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NV; ++i) {
-            mbar_init(v_full + 8 * i, 1);
-            mbar_init(v_empty + 8 * i, NS);  // every scan warp
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(st_full + 8 * i, 1);
+            mbar_init(st_empty + 8 * i, NS);  // every scan warp
         }
         for (int i = 0; i < NL; ++i) mbar_init(qkg_full + 8 * i, 1);
-        for (int i = 0; i < NI; ++i) {
-            mbar_init(imp_full + 8 * i, 1);
-            mbar_init(imp_empty + 8 * i, NS);
-        }
         for (int i = 0; i < NG; ++i) {
             mbar_init(ready + 8 * i, 1);   // the owner's prep lane
             mbar_init(gfree + 8 * i, VS);  // the feeder of every CTA of the cluster
@@ -134,35 +134,29 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
         if (lane == 0) {
             // -------------------------------------------- feeder: V tile and import of every chunk
             tma_prefetch_desc(&tv);
-            int nv = 0, ni = 0;  // V tiles and imports issued
+            int issued = 0;
             for (int n = 0; n < nch; ++n) {
-                const int s = n % NV;
-                if (!wait_bar(v_empty + 8 * s, ((n / NV) & 1) ^ 1, flags)) break;
-                const uint32_t fb = v_full + 8 * s;
-                mbar_arrive_expect_tx(fb, RAW_TILE);
-                const int tok = sp.bos + n * CHUNK;
-                const uint32_t dst = sb + OFF_V + s * RAW_TILE;
-#pragma unroll
-                for (int b = 0; b < 2; ++b) tma_load_3d(dst + b * RAW_BOX, &tv, 64 * b, h, tok, fb);
-                nv = n + 1;
-                const int si = n % NI, e = n % NG;
-                if (!wait_bar(imp_empty + 8 * si, ((n / NI) & 1) ^ 1, flags)) break;
-                if (n >= NI) {  // chunk n - NI has left slot si: its owner may reuse the workspace entry
+                const int s = n % NST, e = n % NG;
+                if (!wait_bar(st_empty + 8 * s, ((n / NST) & 1) ^ 1, flags)) break;
+                if (n >= NST) {  // chunk n - NST has left stage s: its owner may reuse the workspace entry
                     // (the copy's reads completed before its transaction count did, so there is
                     // nothing to release: the arrival is relaxed)
-                    const int m = n - NI;
+                    const int m = n - NST;
                     mbar_arrive_cluster_relaxed(mapa_shared(gfree + 8 * (m % NG), static_cast<uint32_t>(m % VS)));
                 }
                 if (!wait_cluster(ready + 8 * e, (n / NG) & 1, flags)) break;
                 fence_proxy_async_global();  // the owner's generic writes, seen by this thread's bulk copy
-                const uint32_t ib = imp_full + 8 * si;
-                mbar_arrive_expect_tx(ib, PREP_SLOT);
-                bulk_load_global(sb + OFF_IMP + si * PREP_SLOT, wsu + static_cast<size_t>(e) * PREP_SLOT, PREP_SLOT, ib);
-                ni = n + 1;
+                const uint32_t fb = st_full + 8 * s, dst = sb + OFF_STG + s * STAGE;
+                mbar_arrive_expect_tx(fb, RAW_TILE + PREP_SLOT);
+                const int tok = sp.bos + n * CHUNK;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) tma_load_3d(dst + b * RAW_BOX, &tv, 64 * b, h, tok, fb);
+                bulk_load_global(dst + RAW_TILE, wsu + static_cast<size_t>(e) * PREP_SLOT, PREP_SLOT, fb);
+                issued = n + 1;
             }
             // no copy is left in flight when the CTA exits
-            for (int m = (nv > NV ? nv - NV : 0); m < nv; ++m) drain_bar(v_full + 8 * (m % NV), (m / NV) & 1);
-            for (int m = (ni > NI ? ni - NI : 0); m < ni; ++m) drain_bar(imp_full + 8 * (m % NI), (m / NI) & 1);
+            for (int m = (issued > NST ? issued - NST : 0); m < issued; ++m)
+                drain_bar(st_full + 8 * (m % NST), (m / NST) & 1);
         }
     } else if (warp < 1 + 2 * NL) {
         // ------------------------------------------------------------ prep lanes: own chunks
@@ -364,15 +358,17 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
             }
 
         const int mi = lane >> 3, ri = lane & 7;
+        const uint32_t ot = sb + OFF_OT + sw * OT_BYTES;  // this warp's output tile
+        // ldmatrix / stmatrix row addresses: lane 8 i + r names row r of 8x8 matrix i, i.e. token
+        // r + 8 (i >> 1) of the V-row block 8 (i & 1) of this warp's 16 rows
+        const int mtok = (lane & 7) + 8 * (lane >> 4), mcol = 8 * ((lane >> 3) & 1);
         for (int n = 0; n < nch; ++n) {
-            const int si = n % NI, vsl = n % NV;
-            bool ok = wait_bar(imp_full + 8 * si, (n / NI) & 1, flags);
-            ok = ok && wait_bar(v_full + 8 * vsl, (n / NV) & 1, flags);
+            const int si = n % NST;
+            const bool ok = wait_bar(st_full + 8 * si, (n / NST) & 1, flags);
             if (!__all_sync(0xffffffffu, ok)) break;
-            const uint32_t pb = sb + OFF_IMP + si * PREP_SLOT;
+            const uint32_t vt = sb + OFF_STG + si * STAGE, pb = vt + RAW_TILE;
             const int tok0 = sp.bos + n * CHUNK;
             const int Lv = min(CHUNK, sp.len - n * CHUNK);
-            const uint32_t vt = sb + OFF_V + vsl * RAW_TILE;
 
             // Z = S [K*Gamma ; Q*Gamma]^T  (16 rows x 32 columns per warp)
             float z[4][4];
@@ -393,18 +389,22 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
                 mma_bf16(z[3], a, b2, b3);
             }
 
-            // R = V^T - Z_k (rows past the chunk's end are zero)
+            // R = V^T - Z_k (rows past the chunk's end are zero): V^T in the accumulator layout
+            // straight from the swizzled tile, matrix i = V^T rows 8 (i & 1).., tokens 8 (i >> 1)..
             float R[2][4];
+            {
+                uint32_t vw[4];
+                ldsm_x4_t(vt + raw_off(mtok, vr0 + mcol), vw[0], vw[1], vw[2], vw[3]);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int jj = 8 * nt + 2 * t + (q & 1), vr = vr0 + g + 8 * (q >> 1);
-                    const float vv = jj < Lv ? __uint_as_float(static_cast<uint32_t>(SM_AT(const uint16_t, vt + raw_off(jj, vr))) << 16) : 0.f;
-                    R[nt][q] = vv - z[nt][q];
-                }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(v_empty + 8 * vsl);
+                    for (int q = 0; q < 4; ++q) {
+                        const int jj = 8 * nt + 2 * t + (q & 1);
+                        const uint32_t w = vw[2 * nt + (q >> 1)];
+                        const float vv = jj < Lv ? ((q & 1) ? bf16_hi(w) : bf16_lo(w)) : 0.f;
+                        R[nt][q] = vv - z[nt][q];
+                    }
+            }
 
             // E = R (T diag(beta))^T
             const uint32_t ra[4] = {pack_f16(R[0][0], R[0][1]), pack_f16(R[0][2], R[0][3]), pack_f16(R[1][0], R[1][1]),
@@ -425,14 +425,18 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
                 const uint32_t row = pb + P_PP + (8 * nt + g) * SM_LD + 4 * t;
                 mma_f16(z[2 + nt], ea, SM_AT(const uint32_t, row), SM_AT(const uint32_t, row + 16));
             }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = 8 * nt + 2 * t + (q & 1), vr = vr0 + g + 8 * (q >> 1);
-                    const size_t oi = (static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr;
-                    if (r < Lv && gmem_ok(oi, 1, out_elems(p))) p.out[oi] = f2bf_bits(p.scale * z[2 + nt][q]);
-                }
+            // the 16 x 16 output tile, transposed to [token][V row] in shared memory, then one
+            // 16-byte store per lane (token lane / 2, V rows 8 (lane & 1)..)
+            stsm_x4_t(ot + mtok * OT_LD + 2 * mcol, pack_bf16(p.scale * z[2][0], p.scale * z[2][1]),
+                      pack_bf16(p.scale * z[2][2], p.scale * z[2][3]), pack_bf16(p.scale * z[3][0], p.scale * z[3][1]),
+                      pack_bf16(p.scale * z[3][2], p.scale * z[3][3]));
+            __syncwarp();
+            {
+                const int r = lane >> 1, c8 = 8 * (lane & 1);
+                const uint4 o = SM_AT(const uint4, ot + r * OT_LD + 2 * c8);
+                const size_t oi = (static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr0 + c8;
+                if (r < Lv && gmem_ok(oi, 8, out_elems(p))) *reinterpret_cast<uint4 *>(p.out + oi) = o;
+            }
 
             // S = S Diag(gamma) + E Kbar
 #pragma unroll
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
                 mma_f16(S[2 * m + 1], ea, b2, b3);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(imp_empty + 8 * si);
+            if (lane == 0) mbar_arrive(st_empty + 8 * si);
         }
 
         if (p.fin) {
