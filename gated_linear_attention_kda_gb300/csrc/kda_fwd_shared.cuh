@@ -389,6 +389,31 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
                 mma_bf16(z[3], a, b2, b3);
             }
 
+            // Off the chain to the next chunk (Z -> R -> E -> S update -> next Z): decay S by gamma
+            // now (Z has taken its bf16 copy), and load Kbar, T' and P while Z completes.
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                const float2 gm = SM_AT(const float2, pb + P_GAM + (8 * nt + 2 * t) * 4);
+                S[nt][0] *= gm.x;
+                S[nt][1] *= gm.y;
+                S[nt][2] *= gm.x;
+                S[nt][3] *= gm.y;
+            }
+            uint32_t kbf[8][4], ttf[2][2], ppf[2][2];
+            {
+                const uint32_t kb = pb + P_KB + (ri + 8 * (mi & 1)) * BZ_LD + 16 * (mi >> 1);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) ldsm_x4_t(kb + m * 32, kbf[m][0], kbf[m][1], kbf[m][2], kbf[m][3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t rt = pb + P_TT + (8 * nt + g) * SM_LD + 4 * t, rp = pb + P_PP + (8 * nt + g) * SM_LD + 4 * t;
+                    ttf[nt][0] = SM_AT(const uint32_t, rt);
+                    ttf[nt][1] = SM_AT(const uint32_t, rt + 16);
+                    ppf[nt][0] = SM_AT(const uint32_t, rp);
+                    ppf[nt][1] = SM_AT(const uint32_t, rp + 16);
+                }
+            }
+
             // R = V^T - Z_k (rows past the chunk's end are zero): V^T in the accumulator layout
             // straight from the swizzled tile, matrix i = V^T rows 8 (i & 1).., tokens 8 (i >> 1)..
             float R[2][4];
@@ -413,18 +438,21 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 ev[nt][0] = ev[nt][1] = ev[nt][2] = ev[nt][3] = 0.f;
-                const uint32_t row = pb + P_TT + (8 * nt + g) * SM_LD + 4 * t;
-                mma_f16(ev[nt], ra, SM_AT(const uint32_t, row), SM_AT(const uint32_t, row + 16));
+                mma_f16(ev[nt], ra, ttf[nt][0], ttf[nt][1]);
             }
             const uint32_t ea[4] = {pack_f16(ev[0][0], ev[0][1]), pack_f16(ev[0][2], ev[0][3]), pack_f16(ev[1][0], ev[1][1]),
                                     pack_f16(ev[1][2], ev[1][3])};
 
+            // S = S Diag(gamma) + E Kbar (the decay above): issued first, the next chunk waits on it
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                mma_f16(S[2 * m], ea, kbf[m][0], kbf[m][1]);
+                mma_f16(S[2 * m + 1], ea, kbf[m][2], kbf[m][3]);
+            }
+
             // O = scale (Z_q + E P^T)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t row = pb + P_PP + (8 * nt + g) * SM_LD + 4 * t;
-                mma_f16(z[2 + nt], ea, SM_AT(const uint32_t, row), SM_AT(const uint32_t, row + 16));
-            }
+            for (int nt = 0; nt < 2; ++nt) mma_f16(z[2 + nt], ea, ppf[nt][0], ppf[nt][1]);
             // the 16 x 16 output tile, transposed to [token][V row] in shared memory, then one
             // 16-byte store per lane (token lane / 2, V rows 8 (lane & 1)..)
             stsm_x4_t(ot + mtok * OT_LD + 2 * mcol, pack_bf16(p.scale * z[2][0], p.scale * z[2][1]),
@@ -436,24 +464,6 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
                 const uint4 o = SM_AT(const uint4, ot + r * OT_LD + 2 * c8);
                 const size_t oi = (static_cast<size_t>(tok0 + r) * p.H + h) * DH + vr0 + c8;
                 if (r < Lv && gmem_ok(oi, 8, out_elems(p))) *reinterpret_cast<uint4 *>(p.out + oi) = o;
-            }
-
-            // S = S Diag(gamma) + E Kbar
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                const float2 gm = SM_AT(const float2, pb + P_GAM + (8 * nt + 2 * t) * 4);
-                S[nt][0] *= gm.x;
-                S[nt][1] *= gm.y;
-                S[nt][2] *= gm.x;
-                S[nt][3] *= gm.y;
-            }
-            const uint32_t kb = pb + P_KB + (ri + 8 * (mi & 1)) * BZ_LD + 16 * (mi >> 1);
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(kb + m * 32, b0, b1, b2, b3);
-                mma_f16(S[2 * m], ea, b0, b1);
-                mma_f16(S[2 * m + 1], ea, b2, b3);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(st_empty + 8 * si);
