@@ -311,11 +311,12 @@ def test_no_writes_outside_out_and_final_state(H):
 
 # ------------------------------------------------------------ full-size workloads
 
-def _check_every_head(name, final_dtype, group):
+def _check_every_head(name, final_dtype, group, workspace=False):
     """A full-size workload in the launch configuration the benchmark times, compared with the
     oracle on EVERY token of EVERY head. The oracle runs in head groups (heads are independent)
     to bound host memory; the relative L2 error is accumulated over the whole tensor and the
-    elementwise bound is checked in every group."""
+    elementwise bound is checked in every group. ``workspace`` runs the call through kda_fwd_ws
+    (the planned split with the preparation shared by each state's cluster)."""
     import gated_linear_attention_kda_gb300 as kda
     from tests.kda_harness import ABS, REL, REL_L2
     d = W.make(name)
@@ -325,8 +326,14 @@ def _check_every_head(name, final_dtype, group):
     out = torch.full_like(c["v"], float("nan"))
     fin = torch.full((nseq, H, 128, 128), float("nan"), device="cuda",
                      dtype=torch.float32 if final_dtype == "fp32" else torch.bfloat16)
-    kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+    args = (c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
             d["lower_bound"], c["initial_state"], fin, c["cu_seqlens"])
+    if workspace:
+        nbytes = kda.workspace_bytes(nseq, H)
+        assert nbytes > 0, "the planned split must share the preparation here"
+        kda.fwd_ws(*args, workspace=torch.empty(nbytes, dtype=torch.uint8, device="cuda"))
+    else:
+        kda.fwd(*args)
     kda.check_device_status()
     out_h, fin_h = out.cpu(), fin.cpu()
     del c, out, fin
@@ -360,6 +367,11 @@ def test_full_varlen_n16_h32_every_head():
 def test_full_long_context_every_head():
     """B=1, T=131072, H=32, fp32 initial and final states: all 32 heads."""
     _check_every_head("b1_t131072_h32", "fp32", group=16)
+
+
+def test_full_long_context_every_head_shared_preparation():
+    """The same through kda_fwd_ws (split 4, each state's cluster sharing the preparation)."""
+    _check_every_head("b1_t131072_h32", "fp32", group=16, workspace=True)
 
 
 # ------------------------------------------------------------ per-step parity (one chunk)
