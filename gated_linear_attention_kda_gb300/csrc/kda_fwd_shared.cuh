@@ -3,8 +3,8 @@
 // n % VS prepares chunk n (gate, cumsum, scaled operand tiles, the chunk matrices A and P, the
 // inverse T = (I + A)^-1) exactly as the warp-MMA kernel's prep lanes do, and publishes the
 // prepared operands to a workspace in global memory (a 16-entry ring per state, read back through
-// L2); every CTA of the cluster, the owner included, copies each chunk's entry into an import
-// slot and scans it from there. Each CTA prepares only 1 / VS of the chunks, and the preparation
+// L2); every CTA of the cluster, the owner included, copies each chunk's entry into a stage
+// beside the chunk's V tile and scans it from there. Each CTA prepares only 1 / VS of the chunks, and the preparation
 // never waits on the scan: a prep lane's staging slot is free again once it is copied out.
 //
 // Per chunk n, owner o = n % VS, workspace entry e = n % NG. Entry e is always written by the same
@@ -12,12 +12,14 @@
 // barrier of an entry is waited on in phase order by a single waiter:
 //   owner   prep lane -> staging slot (shared memory); once every CTA released entry e's previous
 //           chunk (mbarrier `gfree[e]` of the owner, one arrival per CTA): copy the slot to entry
-//           e, fence, and arrive on `ready[e]` of every CTA (release at cluster scope).
+//           e; one thread then fences at cluster scope and arrives (relaxed) on `ready[e]` of
+//           every CTA -- one fence per chunk, where release-qualified arrivals would fence once
+//           per arrival.
 //   all     the feeder thread waits for `ready[e]` (acquire at cluster scope) and bulk-copies
 //           entry e into a stage beside the chunk's V tile; when it reuses that stage NST chunks
-//           later (the copy has long landed and been scanned), it releases entry e on the owner's
-//           `gfree[e]`. The feeder makes no generic stores, so its signal waits for none, and
-//           the scan warps, which do, never signal another CTA.
+//           later (the copy has long landed and been scanned), it releases entry e with a relaxed
+//           arrival on the owner's `gfree[e]` (nothing to order: the copy's reads completed
+//           before its transaction count did). The scan warps never signal another CTA.
 // The imported bytes are the prep lane's, so results equal the warp-MMA kernel's at the same
 // split bit for bit. The rows of S are independent, which is what makes the split exact
 // ("FlashKDA Input Tensor Shapes and DTypes ..." -- "Initial and Final States").
