@@ -35,7 +35,7 @@ BYTES_PER_TOKEN_HEAD = 4 * 256 + 2 + 256     # q, k, v, g in; beta in; out
 FLOPS_PER_CHUNK_HEAD = 3 * 2 * 16 * 128 * 128 + 5 * 2 * 16 * 16 * 128 + 2 * 16 ** 3
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # the device sources the benchmark's kernel (kda_fwd_tc_kernel) is compiled from: counters taken
-# under ncu describe this build only while these files are unchanged
+# under ncu describe the kernel only while these files are unchanged
 KERNEL_SOURCES = ["gated_linear_attention_kda_gb300/csrc/" + f for f in
                   ("kda_fwd_tc.cuh", "kda_common.cuh", "kda_chunk.cuh", "tcgen05.cuh", "ptx.cuh", "kda_debug.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_fwd_tc_kernel.b8_t4096_h16.traffic.json")
