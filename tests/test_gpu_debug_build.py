@@ -37,11 +37,14 @@ def test_checked_build_catches_an_out_of_range_index_without_the_access():
 
 def test_parity_suites_pass_through_the_checked_build():
     """Every parity test except the full-size ones (their oracle time dominates), including the
-    per-step slot checks of the tcgen05 kernel, through libkda_debug.so."""
+    per-step slot checks of the tcgen05 kernel and the shared-preparation kernel's cases, through
+    libkda_debug.so."""
     r = _run(["-m", "pytest", "-q", "-x", "-m", "gpu", "-k", "not full", "-p", "no:cacheprovider",
               "tests/test_gpu_parity.py", "tests/test_gpu_chunk32.py", "tests/test_gpu_slot_steps.py",
-              "tests/test_gpu_failure_paths.py"], timeout=1800)
+              "tests/test_gpu_shared_prep.py", "tests/test_gpu_failure_paths.py"], timeout=1800)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
     import re
     m = re.search(r"(\d+) passed", r.stdout)
-    assert m and int(m.group(1)) >= 100, r.stdout[-2000:]  # the suites ran, not an empty selection
+    # the suites ran in full (145 tests at the time of writing, 24 of them the shared-preparation
+    # kernel's), not an empty or partial selection
+    assert m and int(m.group(1)) >= 140, r.stdout[-2000:]
