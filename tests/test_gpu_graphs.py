@@ -1,7 +1,8 @@
 """The library's launches can be captured in a CUDA graph and replayed: kda_fwd (both forward
-kernels) and kda_decode, after one eager call on the device (the first call configures each
-kernel's shared-memory size and queries the device, host work that is not part of a capture).
-Replays must equal eager calls bit for bit."""
+kernels), kda_fwd_ws (the cluster launch of the shared-preparation kernel, workspace allocated
+before the capture) and kda_decode, after one eager call on the device (the first call configures
+each kernel's shared-memory size and queries the device, host work that is not part of a
+capture). Replays must equal eager calls bit for bit."""
 import pytest
 import torch
 
@@ -10,15 +11,22 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H", [pytest.param(3, id="mma"), pytest.param(80, id="tcgen05")])
-def test_forward_pass_replays_from_a_cuda_graph(H):
+@pytest.mark.parametrize("H,shared", [pytest.param(3, False, id="mma"), pytest.param(80, False, id="tcgen05"),
+                                      pytest.param(3, True, id="shared-preparation")])
+def test_forward_pass_replays_from_a_cuda_graph(H, shared):
     import gated_linear_attention_kda_gb300 as kda
     d = W.make("b2_t128_h8", T=77, H=H, B=1)
     c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     out = torch.empty_like(c["v"])
     fin = torch.empty_like(c["initial_state"])
-    call = lambda: kda.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
-                           d["lower_bound"], c["initial_state"], fin)
+    args = (c["q"], c["k"], c["v"], c["g"], c["beta"], d["scale"], out, c["A_log"], c["dt_bias"],
+            d["lower_bound"], c["initial_state"], fin)
+    if shared:
+        ws = torch.empty(kda.workspace_bytes(1, H), dtype=torch.uint8, device="cuda")
+        assert ws.numel() > 0
+        call = lambda: kda.fwd_ws(*args, workspace=ws)
+    else:
+        call = lambda: kda.fwd(*args)
     call()
     torch.cuda.synchronize()
     kda.check_device_status()
