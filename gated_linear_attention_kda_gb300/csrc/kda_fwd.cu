@@ -183,7 +183,7 @@ static cudaLaunchConfig_t shared_config(int64_t grid, cudaStream_t s, cudaLaunch
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(32 * (1 + 2 * v1s::NL + NS));
+    cfg.blockDim = dim3(v1s::NTHREADS);
     cfg.dynamicSmemBytes = v1s::SMEM_ALLOC;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -24,10 +24,10 @@
 // split bit for bit. The rows of S are independent, which is what makes the split exact
 // ("FlashKDA Input Tensor Shapes and DTypes ..." -- "Initial and Final States").
 //
-// Roles (32 (5 + NS) threads): warp 0 lane 0 the feeder (in chunk order: the V tile and the
-// import of every chunk), warps 1-4 two prep lanes of two warps (alternate own chunks; each
-// lane loads its own q/k/g tiles), warps 5.. NS scan warps of 16 V rows (fp32 state in
-// registers).
+// Roles (9 warps, see NWARPS): warp 0 lane 0 the feeder (in chunk order: the V tile and the
+// import of every chunk), two prep lanes of two warps (alternate own chunks; each lane loads its
+// own q/k/g tiles), NS scan warps of 16 V rows (fp32 state in registers), on sub-partitions of
+// their own.
 #pragma once
 #include "cluster.cuh"
 #include "kda_chunk.cuh"
@@ -87,8 +87,17 @@ static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 // Workspace bytes per state: NG prepared chunks.
 constexpr int64_t workspace_bytes_per_state() { return static_cast<int64_t>(NG) * PREP_SLOT; }
 
+// Warp roles, placed so that scan warps and prep warps sit on different SM sub-partitions (warp
+// w runs on sub-partition w % 4): warp 0 the feeder; warps 4 i + 1 and 4 i + 2 the scan warps
+// (scan warp 2 i and 2 i + 1); warps 3, 4 prep lane 0 and warps 7, 8 prep lane 1. Warps left over
+// at NS < 4 only take part in the cluster barriers.
+constexpr int NWARPS = 9;
+constexpr int NTHREADS = 32 * NWARPS;
+__device__ __forceinline__ int scan_warp_index(int w) { return (w & 3) == 1 || (w & 3) == 2 ? 2 * (w >> 2) + (w & 3) - 1 : -1; }
+__device__ __forceinline__ int prep_lane_of(int w) { return w == 3 || w == 4 ? 0 : (w == 7 || w == 8 ? 1 : -1); }
+
 template <int NS>
-__global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     kda_fwd_shared_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const Params p,
                           uint8_t *ws)
@@ -160,10 +169,10 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
             for (int m = (issued > NST ? issued - NST : 0); m < issued; ++m)
                 drain_bar(st_full + 8 * (m % NST), (m / NST) & 1);
         }
-    } else if (warp < 1 + 2 * NL) {
+    } else if (prep_lane_of(warp) >= 0) {
         // ------------------------------------------------------------ prep lanes: own chunks
-        const int ln = (warp - 1) >> 1;
-        const int lt = threadIdx.x - 32 - 64 * ln;  // 0..63
+        const int ln = prep_lane_of(warp);
+        const int lt = threadIdx.x - 32 * (ln == 0 ? 3 : 7);  // 0..63
         const int lw = lt >> 5;
         const uint32_t bar_id = 1 + ln;
         const uint32_t scr = sb + OFF_SCR + ln * SCR;
@@ -331,9 +340,9 @@ __global__ void __launch_bounds__(32 * (1 + 2 * NL + NS), 1)
         }
         // the lane's last load, if it has not been waited for, lands before the CTA exits
         if (lt == 0 && loaded > k) drain_bar(qb, (loaded - 1) & 1);
-    } else {
+    } else if (scan_warp_index(warp) >= 0 && scan_warp_index(warp) < NS) {
         // ---------------------------------------------------------------- scan warps
-        const int sw = warp - (1 + 2 * NL);
+        const int sw = scan_warp_index(warp);
         const int g = lane >> 2, t = lane & 3;
         const int vr0 = rank * (16 * NS) + 16 * sw;
         const size_t st_base = (static_cast<size_t>(seq) * p.H + h) * (DH * DH);
